@@ -1,0 +1,184 @@
+/*
+ * lb.h — C ABI of the GB300 layer-boundary library (liblb.so).
+ *
+ * A layer boundary completes the producer's owed sum, folds it into the residual
+ * stream and prepares the consumer's input ("Layer boundaries", sglang developer
+ * guide, opening section and section "Residual stream").  On one GPU the owed
+ * cross-rank sum is recast as K partial-contribution buffers resident in device
+ * memory; every call below does the whole boundary in one pass over HBM.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - bf16 tensors are raw IEEE bfloat16, row-major, rows contiguous (row stride H).
+ *    gamma is float32 [H].  FP8 codes are OCP E4M3 ("fn": max 448, no infinity).
+ *  - All tensor pointers are DEVICE pointers.  Arrays of pointers (`partials`) and
+ *    the ragged-set metadata are HOST arrays, read during the call only.
+ *  - Ownership: the caller allocates and owns every buffer.  The library allocates
+ *    nothing, keeps no per-call state and never synchronises the stream.
+ *  - Execution: kernels are enqueued asynchronously on `stream` (NULL = the legacy
+ *    default stream).  A returned LB_OK means the launch was enqueued.
+ *  - Arithmetic ("Residual update and input read": the fused add+norm keeps its FP32
+ *    accumulation and normalises it, not a rounded snapshot):
+ *      o[t,h]  = (+0 + p_0[t,h] + p_1[t,h] + ... + p_{K-1}[t,h]) + res[t,h]
+ *                (binary32, left to right; no residual term in the Initial state)
+ *      res'    = bf16_rne(o)
+ *      r_t     = 1 / sqrt(sum_h o[t,h]^2 / H + eps)
+ *      yf      = (o * r_t) * gamma[h]         y = bf16_rne(yf)
+ *      FP8:    scale_t = max_h |yf| / 448,   q = e4m3_rne_satfinite(yf / scale_t)
+ *              (an all-zero row gets scale 0 and codes 0x00)
+ *    res' is bit-identical to a sequential binary32 evaluation; y and the FP8 scale
+ *    differ from it only through the order of the sum of squares.
+ *  - Aliasing: residual_out may equal residual_in (in-place fold).  Any other
+ *    overlap between an output and any buffer is rejected (LB_ERR_INVALID_ARGUMENT).
+ *  - Alignment: every tensor pointer must be 16-byte aligned and H a multiple of 8,
+ *    else LB_ERR_MISALIGNED / LB_ERR_UNSUPPORTED.
+ *  - Validation before writes: every argument is checked before anything is
+ *    launched; on any error nothing is written ("Fusion providers and output
+ *    decisions": a candidate that declines must do so before touching its inputs).
+ *  - Empty batch: zero rows returns LB_OK and launches nothing ("Enter and leave the
+ *    layer stack": an empty batch still completes owed work and skips the norm).
+ */
+#ifndef LB_H
+#define LB_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream. */
+struct CUstream_st;
+typedef struct CUstream_st *lb_stream_t;
+
+#define LB_MAX_K 16       /* partial buffers per call */
+#define LB_MAX_TOPK 16    /* routed experts per token in the MoE finalize */
+#define LB_MAX_SETS 64    /* token sets in a ragged batch */
+#define LB_MAX_H 131072   /* hidden size */
+
+typedef enum {
+    LB_OK = 0,
+    LB_ERR_INVALID_ARGUMENT = 1, /* NULL where a buffer is required, bad sizes, overlap */
+    LB_ERR_MISALIGNED = 2,       /* a tensor pointer is not 16-byte aligned */
+    LB_ERR_UNSUPPORTED = 3,      /* K, topk, sets or H outside the supported range */
+    LB_ERR_CUDA = 4              /* the CUDA launch failed; see lb_last_cuda_error() */
+} lb_status;
+
+/* Static, human-readable name of a status. */
+const char *lb_status_string(lb_status status);
+
+/* cudaError_t value of the most recent LB_ERR_CUDA on the calling thread (0 if none). */
+int lb_last_cuda_error(void);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int lb_version(void);
+
+/*
+ * Launch shape that the library uses for `rows` rows of width H on a GPU with
+ * `num_sms` SMs: threads per CTA, 16-byte vectors per thread and CTAs per row (a
+ * thread-block cluster splits a row when there are too few rows to fill the GPU).
+ * Host-only; returns LB_ERR_UNSUPPORTED for an H no shape covers.
+ */
+lb_status lb_launch_shape(int64_t rows, int64_t H, int num_sms, int *threads,
+                          int *vectors_per_thread, int *ctas_per_row);
+
+/*
+ * lb_fold_norm — complete K partial sums, fold into the residual, RMSNorm read.
+ * "Layer boundaries": section "Residual stream" (state table and the helpers
+ * complete_output / fold) and section "Residual update and input read" (fused
+ * update_and_read); "SGLang flashinfer_allreduce_fusion精读", section forward
+ * (all-reduce + residual add + RMSNorm in one kernel at fusion points A and B).
+ *
+ *   partials     host array of K device pointers, each bf16 [T,H]; K in [0, LB_MAX_K]
+ *   residual_in  bf16 [T,H], or NULL for the Initial state (o = sum of partials)
+ *   residual_out bf16 [T,H] receives bf16(o), or NULL to skip (read-only boundary)
+ *   gamma        float32 [H]; required when y_out is given
+ *   y_out        bf16 [T,H] receives the RMSNorm read, or NULL for no read
+ *   T, H         rows and hidden size; T >= 0, 8 <= H <= LB_MAX_H, H % 8 == 0
+ *   eps          >= 0 and finite
+ *
+ * The stream operations of the Residual stream section map to argument patterns:
+ *   enter (Initial)     residual_in = NULL
+ *   complete_output     residual_in = NULL, y_out = NULL  (residual_out = the sum)
+ *   fold                residual_in != NULL, y_out = NULL
+ *   read (Written)      K = 0, residual_out = NULL
+ *   fold + read         every buffer given (the hot path)
+ * K = 0 needs residual_in; at least one of residual_out, y_out must be given.
+ */
+lb_status lb_fold_norm(const void *const *partials, int K, const void *residual_in,
+                       void *residual_out, const float *gamma, void *y_out, int64_t T,
+                       int64_t H, float eps, lb_stream_t stream);
+
+/*
+ * lb_fold_norm_fp8 — lb_fold_norm whose read is quantised per token to FP8 E4M3
+ * with a dynamic scale ("Layer boundaries", section "Execute a layer": prepare()
+ * returns input in the consumer read's format, which can be quantized).
+ *
+ *   q_out        uint8 [T,H] E4M3 codes (required)
+ *   scale_out    float32 [T] per-token scale, max|yf| / 448 (required)
+ *   y_out        bf16 [T,H] unquantised read, or NULL
+ * Other arguments as lb_fold_norm; gamma is required.
+ */
+lb_status lb_fold_norm_fp8(const void *const *partials, int K, const void *residual_in,
+                           void *residual_out, const float *gamma, uint8_t *q_out,
+                           float *scale_out, void *y_out, int64_t T, int64_t H, float eps,
+                           lb_stream_t stream);
+
+/*
+ * lb_moe_finalize_fold_norm — deferred MoE finalize fused with the fold and read.
+ * "Layer boundaries": section "Producer contracts and output state" (HandoffOutput,
+ * a deferred MoE finalize consumed by the next boundary) and section "Enter and
+ * leave the layer stack" (finalize(handoff, residual, gamma) fuses finalize,
+ * all-reduce, residual add and norm).
+ *
+ *   o[t,h] = (+0 + w[t,0]*E[idx[t,0],h] + ... + w[t,topk-1]*E[idx[t,topk-1],h])
+ *            + res[t,h]      (each product rounded to binary32, then added)
+ *
+ *   expert_out     bf16 [n_expert_rows, H], expert-sorted rows of the routed tokens
+ *   idx            int32 [T, topk], row of expert_out for (token, slot)
+ *   w              float32 [T, topk], routing weights
+ *   topk           1 .. LB_MAX_TOPK
+ *   residual_in    bf16 [T,H] or NULL (Initial);  residual_out bf16 [T,H] or NULL
+ *   y_out          bf16 [T,H] or NULL;  q_out uint8 [T,H] + scale_out float32 [T]
+ *                  together or both NULL (FP8 read)
+ *   bad_index_flag int32 device word or NULL.  An index outside [0, n_expert_rows)
+ *                  is skipped (contributes nothing) and, when the flag is given, the
+ *                  kernel stores 1 into it; the caller zeroes it beforehand.
+ */
+lb_status lb_moe_finalize_fold_norm(const void *expert_out, int64_t n_expert_rows,
+                                    const int32_t *idx, const float *w, int topk,
+                                    const void *residual_in, void *residual_out,
+                                    const float *gamma, void *y_out, uint8_t *q_out,
+                                    float *scale_out, int64_t T, int64_t H, float eps,
+                                    int32_t *bad_index_flag, lb_stream_t stream);
+
+/*
+ * lb_slice_fold_norm — one rank's row slice of a padded, ragged token batch after a
+ * fixed-size reduce-scatter ("Layer boundaries", section "Choose a reduction
+ * policy", value rs, and section "Token layouts and sums": ATTN_DP token sets whose
+ * padding and counts come from batch metadata; "SGLang flashinfer_allreduce_fusion
+ * 精读", section forward: with reduce-scatter RMSNorm runs on the rank's slice only).
+ *
+ *   partials       K device pointers, each bf16 [T_pad,H] over the padded batch
+ *   T_pad          padded rows; num_slices >= 1 divides T_pad; S = T_pad/num_slices
+ *   slice          0 <= slice < num_slices; global rows [slice*S, (slice+1)*S)
+ *   set_offsets    host int32 [num_sets]: first padded row of each token set
+ *   set_counts     host int32 [num_sets]: valid rows of each set; set i holds valid
+ *                  rows [offset_i, offset_i + count_i); sets ascending, disjoint,
+ *                  inside [0, T_pad).  num_sets = 0: every row is valid.
+ *   residual_in    bf16 [S,H] compact slice rows, or NULL (Initial)
+ *   residual_out, y_out, q_out/scale_out: compact [S,...] outputs as above
+ * Padding rows are neither computed nor written: their output bytes are untouched.
+ */
+lb_status lb_slice_fold_norm(const void *const *partials, int K, int64_t T_pad,
+                             int num_slices, int slice, const int32_t *set_offsets,
+                             const int32_t *set_counts, int num_sets,
+                             const void *residual_in, void *residual_out,
+                             const float *gamma, void *y_out, uint8_t *q_out,
+                             float *scale_out, int64_t H, float eps, lb_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LB_H */

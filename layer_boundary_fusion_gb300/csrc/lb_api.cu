@@ -1,0 +1,364 @@
+// C-ABI entry points of liblb.so: argument validation, launch shape, dispatch.
+//
+// Every check runs before anything is enqueued, so a rejected call writes nothing
+// ("Layer boundaries", section "Fusion providers and output decisions": a candidate
+// that declines must do so before modifying inputs).  The contract of each entry
+// point is documented in include/lb.h.
+#include <cmath>
+#include <cstdint>
+#include <climits>
+#include <cstring>
+
+#include "lb_internal.h"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+enum BufId { kOther = 0, kResIn = 1, kResOut = 2 };
+
+struct Buf {
+    const void *ptr;
+    uint64_t bytes;
+    bool output;
+    int id;
+};
+
+struct BufList {
+    Buf b[LB_MAX_K + 16];
+    int n = 0;
+    void add(const void *ptr, uint64_t bytes, bool output, int id = kOther) {
+        b[n++] = Buf{ptr, bytes, output, id};
+    }
+};
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// An output may not overlap any other buffer, except residual_out == residual_in
+// (the in-place fold, element for element).
+lb_status check_overlaps(const BufList &l) {
+    for (int i = 0; i < l.n; ++i) {
+        const Buf &o = l.b[i];
+        if (!o.output || o.ptr == nullptr || o.bytes == 0)
+            continue;
+        const uintptr_t o0 = reinterpret_cast<uintptr_t>(o.ptr), o1 = o0 + o.bytes;
+        for (int j = 0; j < l.n; ++j) {
+            const Buf &x = l.b[j];
+            if (j == i || x.ptr == nullptr || x.bytes == 0)
+                continue;
+            const uintptr_t x0 = reinterpret_cast<uintptr_t>(x.ptr), x1 = x0 + x.bytes;
+            if (o0 >= x1 || x0 >= o1)
+                continue;
+            const bool in_place = ((o.id == kResOut && x.id == kResIn) ||
+                                   (o.id == kResIn && x.id == kResOut)) &&
+                                  o0 == x0 && o.bytes == x.bytes;
+            if (!in_place)
+                return LB_ERR_INVALID_ARGUMENT;
+        }
+    }
+    return LB_OK;
+}
+
+lb_status check_shape(int64_t T, int64_t H, float eps) {
+    if (T < 0 || H <= 0 || !(eps >= 0.0f) || !std::isfinite(eps))
+        return LB_ERR_INVALID_ARGUMENT;
+    if (H % 8 != 0 || H > LB_MAX_H)
+        return LB_ERR_UNSUPPORTED;
+    if (T > (int64_t(1) << 27))          // grid: rows x 8 CTAs must fit in 2^31 - 1
+        return LB_ERR_UNSUPPORTED;
+    return LB_OK;
+}
+
+lb_status check_tensor(const void *p) {
+    return aligned(p, 16) ? LB_OK : LB_ERR_MISALIGNED;
+}
+
+#define LB_TRY(expr)                       \
+    do {                                   \
+        const lb_status s_ = (expr);       \
+        if (s_ != LB_OK)                   \
+            return s_;                     \
+    } while (0)
+
+int device_sm_count(int *out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(out, cudaDevAttrMultiProcessorCount, dev);
+    return static_cast<int>(e);
+}
+
+lb_status launch(const lb::Params &p, lb::Mode mode, bool fp8, cudaStream_t stream) {
+    int sms = 0;
+    const int e0 = device_sm_count(&sms);
+    if (e0 != 0) {
+        g_last_cuda_error = e0;
+        return LB_ERR_CUDA;
+    }
+    lb::Shape s;
+    if (!lb::choose_shape(p.rows, p.H, sms, &s))
+        return LB_ERR_UNSUPPORTED;
+    lb::Params q = p;
+    q.vec_per_cta = static_cast<int>(((p.H / 8) + s.ctas_per_row - 1) / s.ctas_per_row);
+    const cudaError_t e = (mode == lb::kFold) ? lb::launch_fold(q, s, fp8, stream)
+                                              : lb::launch_moe(q, s, fp8, stream);
+    if (e != cudaSuccess) {
+        g_last_cuda_error = static_cast<int>(e);
+        return LB_ERR_CUDA;
+    }
+    return LB_OK;
+}
+
+// Shared validation of the fold family (dense and slice).
+lb_status check_fold_inputs(const void *const *partials, int K, int64_t rows_in,
+                            const void *residual_in, BufList *l, int64_t H) {
+    if (K < 0)
+        return LB_ERR_INVALID_ARGUMENT;
+    if (K > LB_MAX_K)
+        return LB_ERR_UNSUPPORTED;
+    if (K > 0 && partials == nullptr)
+        return LB_ERR_INVALID_ARGUMENT;
+    if (K == 0 && residual_in == nullptr)
+        return LB_ERR_INVALID_ARGUMENT;    // nothing to read
+    for (int k = 0; k < K; ++k) {
+        if (partials[k] == nullptr)
+            return LB_ERR_INVALID_ARGUMENT;
+        LB_TRY(check_tensor(partials[k]));
+        l->add(partials[k], static_cast<uint64_t>(rows_in * H * 2), false);
+    }
+    return LB_OK;
+}
+
+// Residual, gamma and outputs of a call that produces `rows` rows.
+lb_status check_stream_buffers(const void *residual_in, void *residual_out,
+                               const float *gamma, void *y_out, uint8_t *q_out,
+                               float *scale_out, int64_t rows, int64_t H, BufList *l) {
+    const bool fp8 = q_out != nullptr || scale_out != nullptr;
+    if (fp8 && (q_out == nullptr || scale_out == nullptr))
+        return LB_ERR_INVALID_ARGUMENT;
+    if (residual_out == nullptr && y_out == nullptr && !fp8)
+        return LB_ERR_INVALID_ARGUMENT;    // nothing to produce
+    if ((y_out != nullptr || fp8) && gamma == nullptr)
+        return LB_ERR_INVALID_ARGUMENT;
+    const uint64_t row_bytes = static_cast<uint64_t>(rows * H * 2);
+    for (const void *t : {residual_in, static_cast<const void *>(residual_out),
+                          static_cast<const void *>(gamma), static_cast<const void *>(y_out),
+                          static_cast<const void *>(q_out)})
+        if (t != nullptr)
+            LB_TRY(check_tensor(t));
+    if (scale_out != nullptr && !aligned(scale_out, 4))
+        return LB_ERR_MISALIGNED;
+    l->add(residual_in, row_bytes, false, kResIn);
+    l->add(residual_out, row_bytes, true, kResOut);
+    if (y_out != nullptr || fp8)
+        l->add(gamma, static_cast<uint64_t>(H * 4), false);
+    l->add(y_out, row_bytes, true);
+    l->add(q_out, static_cast<uint64_t>(rows * H), true);
+    l->add(scale_out, static_cast<uint64_t>(rows * 4), true);
+    return LB_OK;
+}
+
+void set_stream_params(lb::Params *p, const void *residual_in, void *residual_out,
+                       const float *gamma, void *y_out, uint8_t *q_out, float *scale_out,
+                       int64_t rows, int64_t H, float eps) {
+    p->residual_in = static_cast<const uint16_t *>(residual_in);
+    p->residual_out = static_cast<uint16_t *>(residual_out);
+    p->gamma = gamma;
+    p->y_out = static_cast<uint16_t *>(y_out);
+    p->q_out = q_out;
+    p->scale_out = scale_out;
+    p->rows = rows;
+    p->H = H;
+    p->eps = eps;
+}
+
+lb_status fold_common(const void *const *partials, int K, const void *residual_in,
+                      void *residual_out, const float *gamma, void *y_out, uint8_t *q_out,
+                      float *scale_out, int64_t T, int64_t H, float eps,
+                      lb_stream_t stream) {
+    LB_TRY(check_shape(T, H, eps));
+    BufList l;
+    LB_TRY(check_fold_inputs(partials, K, T, residual_in, &l, H));
+    LB_TRY(check_stream_buffers(residual_in, residual_out, gamma, y_out, q_out, scale_out, T,
+                                H, &l));
+    LB_TRY(check_overlaps(l));
+    if (T == 0)
+        return LB_OK;
+    lb::Params p;
+    std::memset(&p, 0, sizeof p);
+    for (int k = 0; k < K; ++k)
+        p.partials[k] = static_cast<const uint16_t *>(partials[k]);
+    p.K = K;
+    set_stream_params(&p, residual_in, residual_out, gamma, y_out, q_out, scale_out, T, H,
+                      eps);
+    return launch(p, lb::kFold, q_out != nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+namespace lb {
+
+bool choose_shape(int64_t rows, int64_t H, int num_sms, Shape *out) {
+    if (rows < 0 || H <= 0 || H % 8 != 0 || num_sms <= 0)
+        return false;
+    const int64_t nvec = H / 8;
+    // Split rows across a cluster while the rows alone would leave the GPU under two
+    // CTAs per SM, keeping at least 64 vectors (two warps) per CTA.
+    int cs = 1;
+    while (cs < 8 && rows * cs < 2 * static_cast<int64_t>(num_sms) && nvec / (2 * cs) >= 64)
+        cs *= 2;
+    // Long rows: at most 512 threads x 4 vectors per CTA.
+    while (cs < 8 && (nvec + cs - 1) / cs > 2048)
+        cs *= 2;
+    const int64_t vpc = (nvec + cs - 1) / cs;
+    if (vpc > 2048)
+        return false;
+    const int vpt = vpc <= 512 ? 1 : (vpc <= 1024 ? 2 : 4);
+    int64_t threads = (vpc + vpt - 1) / vpt;
+    threads = ((threads + 31) / 32) * 32;
+    out->threads = static_cast<int>(threads);
+    out->vpt = vpt;
+    out->ctas_per_row = cs;
+    return true;
+}
+
+}  // namespace lb
+
+extern "C" {
+
+const char *lb_status_string(lb_status status) {
+    switch (status) {
+    case LB_OK: return "LB_OK";
+    case LB_ERR_INVALID_ARGUMENT: return "LB_ERR_INVALID_ARGUMENT";
+    case LB_ERR_MISALIGNED: return "LB_ERR_MISALIGNED";
+    case LB_ERR_UNSUPPORTED: return "LB_ERR_UNSUPPORTED";
+    case LB_ERR_CUDA: return "LB_ERR_CUDA";
+    }
+    return "LB_ERR_UNKNOWN";
+}
+
+int lb_last_cuda_error(void) { return g_last_cuda_error; }
+
+int lb_version(void) { return 100; }
+
+lb_status lb_launch_shape(int64_t rows, int64_t H, int num_sms, int *threads,
+                          int *vectors_per_thread, int *ctas_per_row) {
+    if (threads == nullptr || vectors_per_thread == nullptr || ctas_per_row == nullptr)
+        return LB_ERR_INVALID_ARGUMENT;
+    lb::Shape s;
+    if (!lb::choose_shape(rows, H, num_sms, &s))
+        return LB_ERR_UNSUPPORTED;
+    *threads = s.threads;
+    *vectors_per_thread = s.vpt;
+    *ctas_per_row = s.ctas_per_row;
+    return LB_OK;
+}
+
+lb_status lb_fold_norm(const void *const *partials, int K, const void *residual_in,
+                       void *residual_out, const float *gamma, void *y_out, int64_t T,
+                       int64_t H, float eps, lb_stream_t stream) {
+    return fold_common(partials, K, residual_in, residual_out, gamma, y_out, nullptr,
+                       nullptr, T, H, eps, stream);
+}
+
+lb_status lb_fold_norm_fp8(const void *const *partials, int K, const void *residual_in,
+                           void *residual_out, const float *gamma, uint8_t *q_out,
+                           float *scale_out, void *y_out, int64_t T, int64_t H, float eps,
+                           lb_stream_t stream) {
+    if (q_out == nullptr || scale_out == nullptr)
+        return LB_ERR_INVALID_ARGUMENT;
+    return fold_common(partials, K, residual_in, residual_out, gamma, y_out, q_out,
+                       scale_out, T, H, eps, stream);
+}
+
+lb_status lb_moe_finalize_fold_norm(const void *expert_out, int64_t n_expert_rows,
+                                    const int32_t *idx, const float *w, int topk,
+                                    const void *residual_in, void *residual_out,
+                                    const float *gamma, void *y_out, uint8_t *q_out,
+                                    float *scale_out, int64_t T, int64_t H, float eps,
+                                    int32_t *bad_index_flag, lb_stream_t stream) {
+    LB_TRY(check_shape(T, H, eps));
+    if (topk < 1 || n_expert_rows < 0)
+        return LB_ERR_INVALID_ARGUMENT;
+    if (topk > LB_MAX_TOPK || n_expert_rows > (int64_t(1) << 31))
+        return LB_ERR_UNSUPPORTED;
+    if (expert_out == nullptr || idx == nullptr || w == nullptr)
+        return LB_ERR_INVALID_ARGUMENT;
+    LB_TRY(check_tensor(expert_out));
+    if (!aligned(idx, 4) || !aligned(w, 4) ||
+        (bad_index_flag != nullptr && !aligned(bad_index_flag, 4)))
+        return LB_ERR_MISALIGNED;
+    BufList l;
+    l.add(expert_out, static_cast<uint64_t>(n_expert_rows * H * 2), false);
+    l.add(idx, static_cast<uint64_t>(T * topk * 4), false);
+    l.add(w, static_cast<uint64_t>(T * topk * 4), false);
+    l.add(bad_index_flag, 4, true);
+    LB_TRY(check_stream_buffers(residual_in, residual_out, gamma, y_out, q_out, scale_out, T,
+                                H, &l));
+    LB_TRY(check_overlaps(l));
+    if (T == 0)
+        return LB_OK;
+    lb::Params p;
+    std::memset(&p, 0, sizeof p);
+    p.expert_out = static_cast<const uint16_t *>(expert_out);
+    p.n_expert_rows = n_expert_rows;
+    p.idx = idx;
+    p.w = w;
+    p.topk = topk;
+    p.bad_index = bad_index_flag;
+    set_stream_params(&p, residual_in, residual_out, gamma, y_out, q_out, scale_out, T, H,
+                      eps);
+    return launch(p, lb::kMoe, q_out != nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+lb_status lb_slice_fold_norm(const void *const *partials, int K, int64_t T_pad,
+                             int num_slices, int slice, const int32_t *set_offsets,
+                             const int32_t *set_counts, int num_sets,
+                             const void *residual_in, void *residual_out,
+                             const float *gamma, void *y_out, uint8_t *q_out,
+                             float *scale_out, int64_t H, float eps, lb_stream_t stream) {
+    if (T_pad < 0 || num_slices < 1 || T_pad % num_slices != 0 || slice < 0 ||
+        slice >= num_slices || num_sets < 0)
+        return LB_ERR_INVALID_ARGUMENT;
+    if (num_sets > LB_MAX_SETS || T_pad > INT32_MAX)
+        return LB_ERR_UNSUPPORTED;
+    if (num_sets > 0 && (set_offsets == nullptr || set_counts == nullptr))
+        return LB_ERR_INVALID_ARGUMENT;
+    int64_t prev_end = 0;
+    for (int s = 0; s < num_sets; ++s) {
+        const int64_t lo = set_offsets[s], n = set_counts[s];
+        if (lo < prev_end || n < 0 || lo + n > T_pad)
+            return LB_ERR_INVALID_ARGUMENT;  // sets must be ascending, disjoint, inside
+        prev_end = lo + n;
+    }
+    const int64_t S = T_pad / num_slices;
+    LB_TRY(check_shape(S, H, eps));
+    BufList l;
+    LB_TRY(check_fold_inputs(partials, K, T_pad, residual_in, &l, H));
+    LB_TRY(check_stream_buffers(residual_in, residual_out, gamma, y_out, q_out, scale_out, S,
+                                H, &l));
+    LB_TRY(check_overlaps(l));
+    if (S == 0)
+        return LB_OK;
+    lb::Params p;
+    std::memset(&p, 0, sizeof p);
+    for (int k = 0; k < K; ++k)
+        p.partials[k] = static_cast<const uint16_t *>(partials[k]);
+    p.K = K;
+    p.in_row0 = static_cast<int64_t>(slice) * S;
+    p.num_sets = num_sets;
+    bool any_valid = num_sets == 0;
+    for (int s = 0; s < num_sets; ++s) {
+        p.set_lo[s] = set_offsets[s];
+        p.set_hi[s] = set_offsets[s] + set_counts[s];
+        any_valid |= (p.set_lo[s] < p.in_row0 + S) && (p.set_hi[s] > p.in_row0) &&
+                     (set_counts[s] > 0);
+    }
+    if (!any_valid)
+        return LB_OK;                          // the slice holds padding only
+    set_stream_params(&p, residual_in, residual_out, gamma, y_out, q_out, scale_out, S, H,
+                      eps);
+    return launch(p, lb::kFold, q_out != nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,188 @@
+"""Thin ctypes binding of ``liblb.so`` (declared in include/lb.h).
+
+Argument marshalling only: every function has the name and argument order of the C
+entry point, turns tensors into device pointers (a ``torch.Tensor``, an integer
+address or ``None`` for NULL are accepted wherever the C side takes a pointer),
+passes the stream, and raises :class:`LBError` on a non-OK status.  All work runs in
+the library's kernels; there is no fallback.  If the library has not been built the
+first call raises :class:`LibraryMissing`.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "liblb.so")
+
+LB_OK = 0
+LB_ERR_INVALID_ARGUMENT = 1
+LB_ERR_MISALIGNED = 2
+LB_ERR_UNSUPPORTED = 3
+LB_ERR_CUDA = 4
+LB_MAX_K = 16
+LB_MAX_TOPK = 16
+LB_MAX_SETS = 64
+LB_MAX_H = 131072
+
+EXPORTED = ("lb_status_string", "lb_last_cuda_error", "lb_version", "lb_launch_shape",
+            "lb_fold_norm", "lb_fold_norm_fp8", "lb_moe_finalize_fold_norm",
+            "lb_slice_fold_norm")
+
+
+class LibraryMissing(RuntimeError):
+    pass
+
+
+class LBError(RuntimeError):
+    def __init__(self, status: int, func: str):
+        self.status = status
+        name = _lib.lb_status_string(status).decode() if _lib else str(status)
+        extra = ""
+        if status == LB_ERR_CUDA and _lib:
+            extra = f" (cudaError {_lib.lb_last_cuda_error()})"
+        super().__init__(f"{func} failed: {name}{extra}")
+
+
+_lib = None
+
+_vp = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_int = ctypes.c_int
+_f32 = ctypes.c_float
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load liblb.so (once).  Raises LibraryMissing when it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise LibraryMissing(
+            f"{path} is missing: build it with `python -m layer_boundary_fusion_gb300.build`")
+    lib = ctypes.CDLL(path)
+    lib.lb_status_string.argtypes = [_int]
+    lib.lb_status_string.restype = ctypes.c_char_p
+    lib.lb_last_cuda_error.argtypes = []
+    lib.lb_last_cuda_error.restype = _int
+    lib.lb_version.argtypes = []
+    lib.lb_version.restype = _int
+    ip = ctypes.POINTER(_int)
+    lib.lb_launch_shape.argtypes = [_i64, _i64, _int, ip, ip, ip]
+    lib.lb_launch_shape.restype = _int
+    lib.lb_fold_norm.argtypes = [ctypes.POINTER(_vp), _int, _vp, _vp, _vp, _vp, _i64, _i64,
+                                 _f32, _vp]
+    lib.lb_fold_norm.restype = _int
+    lib.lb_fold_norm_fp8.argtypes = [ctypes.POINTER(_vp), _int, _vp, _vp, _vp, _vp, _vp, _vp,
+                                     _i64, _i64, _f32, _vp]
+    lib.lb_fold_norm_fp8.restype = _int
+    lib.lb_moe_finalize_fold_norm.argtypes = [_vp, _i64, _vp, _vp, _int, _vp, _vp, _vp, _vp,
+                                              _vp, _vp, _i64, _i64, _f32, _vp, _vp]
+    lib.lb_moe_finalize_fold_norm.restype = _int
+    lib.lb_slice_fold_norm.argtypes = [ctypes.POINTER(_vp), _int, _i64, _int, _int, _vp, _vp,
+                                       _int, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _f32, _vp]
+    lib.lb_slice_fold_norm.restype = _int
+    _lib = lib
+    return lib
+
+
+def _ptr(x) -> Optional[int]:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream, *tensors) -> Optional[int]:
+    """An explicit stream (torch.cuda.Stream or raw handle), else torch's current
+    stream on the device of the first CUDA tensor argument, else the default stream."""
+    if stream is not None:
+        return stream if isinstance(stream, int) else stream.cuda_stream
+    for t in tensors:
+        if t is not None and not isinstance(t, int) and getattr(t, "is_cuda", False):
+            import torch
+            return torch.cuda.current_stream(t.device).cuda_stream
+    return None
+
+
+def _ptr_array(items: Sequence) -> ctypes.Array:
+    arr = (_vp * max(1, len(items)))()
+    for i, x in enumerate(items):
+        arr[i] = _ptr(x)
+    return arr
+
+
+def _check(status: int, func: str) -> None:
+    if status != LB_OK:
+        raise LBError(status, func)
+
+
+def lb_status_string(status: int) -> str:
+    return load().lb_status_string(status).decode()
+
+
+def lb_version() -> int:
+    return load().lb_version()
+
+
+def lb_launch_shape(rows: int, H: int, num_sms: int):
+    """(threads, vectors_per_thread, ctas_per_row) the library launches with."""
+    t, v, c = _int(), _int(), _int()
+    _check(load().lb_launch_shape(rows, H, num_sms, ctypes.byref(t), ctypes.byref(v),
+                                  ctypes.byref(c)), "lb_launch_shape")
+    return t.value, v.value, c.value
+
+
+def lb_fold_norm(partials, residual_in, residual_out, gamma, y_out, T, H, eps,
+                 stream=None) -> None:
+    lib = load()
+    partials = list(partials)
+    s = _stream(stream, *partials, residual_in, residual_out, y_out)
+    _check(lib.lb_fold_norm(_ptr_array(partials), len(partials), _ptr(residual_in),
+                            _ptr(residual_out), _ptr(gamma), _ptr(y_out), T, H, eps, s),
+           "lb_fold_norm")
+
+
+def lb_fold_norm_fp8(partials, residual_in, residual_out, gamma, q_out, scale_out, y_out,
+                     T, H, eps, stream=None) -> None:
+    lib = load()
+    partials = list(partials)
+    s = _stream(stream, *partials, residual_in, residual_out, q_out)
+    _check(lib.lb_fold_norm_fp8(_ptr_array(partials), len(partials), _ptr(residual_in),
+                                _ptr(residual_out), _ptr(gamma), _ptr(q_out),
+                                _ptr(scale_out), _ptr(y_out), T, H, eps, s),
+           "lb_fold_norm_fp8")
+
+
+def lb_moe_finalize_fold_norm(expert_out, n_expert_rows, idx, w, topk, residual_in,
+                              residual_out, gamma, y_out, q_out, scale_out, T, H, eps,
+                              bad_index_flag=None, stream=None) -> None:
+    lib = load()
+    s = _stream(stream, expert_out, residual_out, y_out, q_out)
+    _check(lib.lb_moe_finalize_fold_norm(_ptr(expert_out), n_expert_rows, _ptr(idx), _ptr(w),
+                                         topk, _ptr(residual_in), _ptr(residual_out),
+                                         _ptr(gamma), _ptr(y_out), _ptr(q_out),
+                                         _ptr(scale_out), T, H, eps, _ptr(bad_index_flag),
+                                         s),
+           "lb_moe_finalize_fold_norm")
+
+
+def lb_slice_fold_norm(partials, T_pad, num_slices, slice_, set_offsets, set_counts,
+                       residual_in, residual_out, gamma, y_out, q_out, scale_out, H, eps,
+                       stream=None) -> None:
+    lib = load()
+    partials = list(partials)
+    n = len(set_offsets)
+    if len(set_counts) != n:
+        raise ValueError("set_offsets and set_counts differ in length")
+    offs = (ctypes.c_int32 * max(1, n))(*[int(v) for v in set_offsets])
+    cnts = (ctypes.c_int32 * max(1, n))(*[int(v) for v in set_counts])
+    s = _stream(stream, *partials, residual_out, y_out, q_out)
+    _check(lib.lb_slice_fold_norm(_ptr_array(partials), len(partials), T_pad, num_slices,
+                                  slice_, ctypes.cast(offs, _vp), ctypes.cast(cnts, _vp), n,
+                                  _ptr(residual_in), _ptr(residual_out), _ptr(gamma),
+                                  _ptr(y_out), _ptr(q_out), _ptr(scale_out), H, eps, s),
+           "lb_slice_fold_norm")

@@ -1,0 +1,201 @@
+"""Host-side tests of the C ABI: the library builds and loads, exports exactly what
+include/lb.h declares, chooses launch shapes as documented, and rejects every invalid
+argument before launching anything.
+
+No kernel runs here.  The argument-validation cases use fake device addresses, so
+they execute in a child process that sees no GPU at all: a case that wrongly passed
+validation would get a CUDA "no device" error, never a launch on a bad address.
+"""
+import json
+import os
+import re
+import subprocess
+import sys
+
+import pytest
+
+from conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from layer_boundary_fusion_gb300 import build, lb
+    build.build()
+    return lb
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "lb.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(lb_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_four_boundary_calls():
+    names = declared_functions()
+    for f in ("lb_fold_norm", "lb_fold_norm_fp8", "lb_moe_finalize_fold_norm",
+              "lb_slice_fold_norm"):
+        assert f in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    out = subprocess.run(["nm", "-D", "--defined-only", lib.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\b[TW] (lb_[a-z0-9_]+)$", out, flags=re.M))
+    assert set(names) <= exported, set(names) - exported
+    assert exported == set(lib.EXPORTED), exported ^ set(lib.EXPORTED)
+    L = lib.load()
+    for n in names:
+        assert hasattr(L, n)
+
+
+def test_status_strings_and_version(lib):
+    assert lib.lb_status_string(0) == "LB_OK"
+    assert lib.lb_status_string(4) == "LB_ERR_CUDA"
+    assert lib.lb_version() >= 100
+
+
+def test_header_constants_match_binding(lib):
+    text = open(os.path.join(ROOT, "include", "lb.h")).read()
+    for name in ("LB_MAX_K", "LB_MAX_TOPK", "LB_MAX_SETS", "LB_MAX_H"):
+        m = re.search(rf"#define {name} (\d+)", text)
+        assert int(m.group(1)) == getattr(lib, name)
+
+
+@pytest.mark.parametrize("rows,H,shape", [
+    (2048, 4096, (512, 1, 1)),      # prefill: one CTA per row
+    (1024, 4096, (512, 1, 1)),
+    (64, 4096, (64, 1, 8)),         # decode: an 8-CTA cluster per row
+    (254, 4096, (256, 1, 2)),       # one slice of a ragged batch
+    (1, 4096, (64, 1, 8)),
+    (16, 512, (64, 1, 1)),
+    (4096, 8192, (512, 2, 1)),
+    (4096, 16384, (512, 4, 1)),
+    (4096, 32768, (512, 4, 2)),
+    (4096, 520, (96, 1, 1)),        # 65 vectors: a partly active warp
+    (4096, 8, (32, 1, 1)),
+])
+def test_launch_shape(lib, rows, H, shape):
+    assert lib.lb_launch_shape(rows, H, 152) == shape
+
+
+def test_launch_shape_covers_every_row_vector(lib):
+    for H in list(range(8, 4096, 8)) + [8192, 12288, 16384, 24576, 65536, 131072]:
+        for rows in (1, 7, 64, 300, 5000):
+            t, v, c = lib.lb_launch_shape(rows, H, 152)
+            per_cta = -(-(H // 8) // c)
+            assert t % 32 == 0 and 32 <= t <= 512 and v in (1, 2, 4) and 1 <= c <= 8
+            assert t * v >= per_cta and c * per_cta >= H // 8
+
+
+def test_launch_shape_rejects(lib):
+    for args in ((10, 12, 152), (10, 0, 152), (10, lib.LB_MAX_H + 8, 152), (10, 4096, 0)):
+        with pytest.raises(lib.LBError):
+            lib.lb_launch_shape(*args)
+
+
+_VALIDATION_SCRIPT = r"""
+import json, sys
+sys.path.insert(0, sys.argv[1])
+from layer_boundary_fusion_gb300 import lb
+L = lb.load()
+A = 1 << 32          # fake, 16-byte aligned "device" addresses; nothing dereferences them
+def a(i): return A + i * (1 << 28)
+T, H = 4, 64
+P = [a(0), a(1)]
+results = {}
+def run(name, fn, *args):
+    try:
+        fn(*args); results[name] = 0
+    except lb.LBError as e:
+        results[name] = e.status
+f = lb.lb_fold_norm
+run("ok_empty", f, P, a(2), a(3), a(4), a(5), 0, H, 1e-6, 0)
+results["K_negative"] = L.lb_fold_norm(None, -1, a(2), a(3), a(4), a(5), T, H, 1e-6, None)
+run("K_too_big", f, [a(i) for i in range(17)], a(20), a(21), a(22), a(23), T, H, 1e-6, 0)
+run("partial_null", f, [a(0), None], a(2), a(3), a(4), a(5), T, H, 1e-6, 0)
+run("partial_misaligned", f, [a(0), a(1) + 8], a(2), a(3), a(4), a(5), T, H, 1e-6, 0)
+run("K0_no_residual", f, [], None, a(3), a(4), a(5), T, H, 1e-6, 0)
+run("nothing_to_write", f, P, a(2), None, a(4), None, T, H, 1e-6, 0)
+run("y_without_gamma", f, P, a(2), a(3), None, a(5), T, H, 1e-6, 0)
+run("H_not_multiple_of_8", f, P, a(2), a(3), a(4), a(5), T, 60, 1e-6, 0)
+run("H_zero", f, P, a(2), a(3), a(4), a(5), T, 0, 1e-6, 0)
+run("H_too_big", f, P, a(2), a(3), a(4), a(5), T, lb.LB_MAX_H + 8, 1e-6, 0)
+run("T_negative", f, P, a(2), a(3), a(4), a(5), -1, H, 1e-6, 0)
+run("eps_negative", f, P, a(2), a(3), a(4), a(5), T, H, -1e-6, 0)
+run("eps_nan", f, P, a(2), a(3), a(4), a(5), T, H, float("nan"), 0)
+run("y_misaligned", f, P, a(2), a(3), a(4), a(5) + 2, T, H, 1e-6, 0)
+run("gamma_misaligned", f, P, a(2), a(3), a(4) + 4, a(5), T, H, 1e-6, 0)
+run("y_overlaps_partial", f, P, a(2), a(3), a(4), a(0) + 16, T, H, 1e-6, 0)
+run("y_overlaps_residual_out", f, P, a(2), a(3), a(4), a(3) + 16, T, H, 1e-6, 0)
+run("residual_out_shifted_over_in", f, P, a(2), a(2) + 16, a(4), a(5), T, H, 1e-6, 0)
+run("in_place_empty_ok", f, P, a(2), a(2), a(4), a(5), 0, H, 1e-6, 0)
+g = lb.lb_fold_norm_fp8
+run("fp8_empty_ok", g, P, a(2), a(3), a(4), a(6), a(7), a(5), 0, H, 1e-6, 0)
+run("fp8_no_q", g, P, a(2), a(3), a(4), None, a(7), a(5), T, H, 1e-6, 0)
+run("fp8_no_scale", g, P, a(2), a(3), a(4), a(6), None, a(5), T, H, 1e-6, 0)
+run("fp8_no_gamma", g, P, a(2), a(3), None, a(6), a(7), None, T, H, 1e-6, 0)
+run("fp8_scale_misaligned", g, P, a(2), a(3), a(4), a(6), a(7) + 2, None, T, H, 1e-6, 0)
+run("fp8_q_overlaps_y", g, P, a(2), a(3), a(4), a(6), a(7), a(6), T, H, 1e-6, 0)
+m = lb.lb_moe_finalize_fold_norm
+run("moe_empty_ok", m, a(0), 32, a(1), a(8), 8, a(2), a(3), a(4), a(5), None, None, 0, H, 1e-6, None, 0)
+run("moe_topk0", m, a(0), 32, a(1), a(8), 0, a(2), a(3), a(4), a(5), None, None, T, H, 1e-6, None, 0)
+run("moe_topk_big", m, a(0), 32, a(1), a(8), 17, a(2), a(3), a(4), a(5), None, None, T, H, 1e-6, None, 0)
+run("moe_no_idx", m, a(0), 32, None, a(8), 8, a(2), a(3), a(4), a(5), None, None, T, H, 1e-6, None, 0)
+run("moe_no_w", m, a(0), 32, a(1), None, 8, a(2), a(3), a(4), a(5), None, None, T, H, 1e-6, None, 0)
+run("moe_no_experts", m, None, 32, a(1), a(8), 8, a(2), a(3), a(4), a(5), None, None, T, H, 1e-6, None, 0)
+run("moe_rows_negative", m, a(0), -1, a(1), a(8), 8, a(2), a(3), a(4), a(5), None, None, T, H, 1e-6, None, 0)
+run("moe_idx_misaligned", m, a(0), 32, a(1) + 2, a(8), 8, a(2), a(3), a(4), a(5), None, None, T, H, 1e-6, None, 0)
+run("moe_half_fp8", m, a(0), 32, a(1), a(8), 8, a(2), a(3), a(4), a(5), a(6), None, T, H, 1e-6, None, 0)
+run("moe_flag_in_experts", m, a(0), 32, a(1), a(8), 8, a(2), a(3), a(4), a(5), None, None, T, H, 1e-6, a(0) + 64, 0)
+s = lb.lb_slice_fold_norm
+off, cnt = [0, 40, 552, 560], [37, 512, 5, 1470]
+run("slice_empty_ok", s, P, 0, 8, 0, off[:0], cnt[:0], a(2), a(3), a(4), a(5), None, None, H, 1e-6, 0)
+run("slice_uneven", s, P, 2031, 8, 3, off, cnt, a(2), a(3), a(4), a(5), None, None, H, 1e-6, 0)
+run("slice_index_high", s, P, 2032, 8, 8, off, cnt, a(2), a(3), a(4), a(5), None, None, H, 1e-6, 0)
+run("slice_index_negative", s, P, 2032, 8, -1, off, cnt, a(2), a(3), a(4), a(5), None, None, H, 1e-6, 0)
+run("slice_zero_slices", s, P, 2032, 0, 0, off, cnt, a(2), a(3), a(4), a(5), None, None, H, 1e-6, 0)
+run("slice_sets_overlap", s, P, 2032, 8, 3, [0, 30, 552, 560], cnt, a(2), a(3), a(4), a(5), None, None, H, 1e-6, 0)
+run("slice_sets_descending", s, P, 2032, 8, 3, [560, 552, 40, 0], cnt, a(2), a(3), a(4), a(5), None, None, H, 1e-6, 0)
+run("slice_set_past_end", s, P, 2032, 8, 3, [0, 40, 552, 570], cnt, a(2), a(3), a(4), a(5), None, None, H, 1e-6, 0)
+run("slice_count_negative", s, P, 2032, 8, 3, off, [37, -1, 5, 1470], a(2), a(3), a(4), a(5), None, None, H, 1e-6, 0)
+run("slice_too_many_sets", s, P, 2032, 8, 3, list(range(65)), [0] * 65, a(2), a(3), a(4), a(5), None, None, H, 1e-6, 0)
+run("slice_padding_only_ok", s, P, 2032, 8, 7, [0], [8], a(2), a(3), a(4), a(5), None, None, H, 1e-6, 0)
+print(json.dumps(results))
+"""
+
+EXPECTED = {
+    "ok_empty": 0, "K_negative": 1, "K_too_big": 3, "partial_null": 1,
+    "partial_misaligned": 2, "K0_no_residual": 1, "nothing_to_write": 1,
+    "y_without_gamma": 1, "H_not_multiple_of_8": 3, "H_zero": 1, "H_too_big": 3,
+    "T_negative": 1, "eps_negative": 1, "eps_nan": 1, "y_misaligned": 2,
+    "gamma_misaligned": 2, "y_overlaps_partial": 1, "y_overlaps_residual_out": 1,
+    "residual_out_shifted_over_in": 1, "in_place_empty_ok": 0,
+    "fp8_empty_ok": 0, "fp8_no_q": 1, "fp8_no_scale": 1, "fp8_no_gamma": 1,
+    "fp8_scale_misaligned": 2, "fp8_q_overlaps_y": 1,
+    "moe_empty_ok": 0, "moe_topk0": 1, "moe_topk_big": 3, "moe_no_idx": 1, "moe_no_w": 1,
+    "moe_no_experts": 1, "moe_rows_negative": 1, "moe_idx_misaligned": 2,
+    "moe_half_fp8": 1, "moe_flag_in_experts": 1,
+    "slice_empty_ok": 0, "slice_uneven": 1, "slice_index_high": 1,
+    "slice_index_negative": 1, "slice_zero_slices": 1, "slice_sets_overlap": 1,
+    "slice_sets_descending": 1, "slice_set_past_end": 1, "slice_count_negative": 1,
+    "slice_too_many_sets": 3, "slice_padding_only_ok": 0,
+}
+
+
+def test_invalid_arguments_are_rejected_before_any_launch(lib):
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-c", _VALIDATION_SCRIPT, ROOT], env=env,
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    got = json.loads(r.stdout.strip().splitlines()[-1])
+    assert got == EXPECTED
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    code = ("import sys; sys.path.insert(0, sys.argv[1]);"
+            "from layer_boundary_fusion_gb300 import lb\n"
+            "try:\n    lb.load(sys.argv[2])\nexcept lb.LibraryMissing:\n    print('missing')\n")
+    r = subprocess.run([sys.executable, "-c", code, ROOT, str(tmp_path / "none.so")],
+                       capture_output=True, text=True, timeout=120)
+    assert r.stdout.strip() == "missing"

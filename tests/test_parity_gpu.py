@@ -1,0 +1,331 @@
+"""GPU parity: every entry point of liblb.so, called through the C ABI, against the
+CPU oracle on the same seeded bf16 inputs, element by element.
+
+Covered: the five specified workloads at full size (tiny fold+norm; decode K=8
+T=64 with and without a residual; prefill K=4 T=2048 with the FP8 read; every slice
+of the ragged batch; the MoE finalize), every stream mode (enter, complete_output,
+fold, read, fold+read, in place), the launch shapes (cluster split, 1/2/4 vectors
+per thread, partly active warps), the maximum K and topk, empty batches, zero rows,
+bad expert indices, guard rows around every output and unchanged inputs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from layer_boundary_fusion_gb300 import workloads as wl
+from parity_util import (Guarded, assert_bf16_close, assert_bits_equal, assert_fp8_close,
+                         dev_bits, host_bits, SENTINEL16)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lb():
+    if not torch.cuda.is_available():
+        pytest.fail("a CUDA GPU is required for the parity tests")
+    from layer_boundary_fusion_gb300 import build, lb as binding
+    build.build()
+    binding.load()
+    return binding
+
+
+def _snapshot(ts):
+    return [None if t is None else t.clone() for t in ts]
+
+
+def _assert_unchanged(before, after):
+    for b, a in zip(before, after):
+        if b is not None:
+            assert torch.equal(b.view(torch.int16) if b.dtype == torch.bfloat16 else b,
+                               a.view(torch.int16) if a.dtype == torch.bfloat16 else a), \
+                "an input buffer was modified"
+
+
+def gpu_fold(lb, partials, residual, gamma, eps, *, want_res=True, want_y=True, fp8=False,
+             want_y_fp8=False, in_place=False):
+    T, H = (partials[0] if partials else residual).shape
+    P = [dev_bits(p) for p in partials]
+    R = dev_bits(residual) if residual is not None else None
+    G = torch.from_numpy(np.ascontiguousarray(gamma)).cuda()
+    ro = Guarded(T, H, torch.bfloat16) if want_res and not in_place else None
+    yo = Guarded(T, H, torch.bfloat16) if (want_y and not fp8) or want_y_fp8 else None
+    qo = Guarded(T, H, torch.uint8) if fp8 else None
+    so = Guarded(T, 0, torch.float32) if fp8 else None
+    res_out = R if in_place else (ro.t if ro else None)
+    before = _snapshot(P + [None if in_place else R, G])
+    if fp8:
+        lb.lb_fold_norm_fp8(P, R, res_out, G, qo.t, so.t, yo.t if yo else None, T, H, eps)
+    else:
+        lb.lb_fold_norm(P, R, res_out, G if want_y else None, yo.t if yo else None, T, H, eps)
+    torch.cuda.synchronize()
+    _assert_unchanged(before, P + [None if in_place else R, G])
+    out = {}
+    for name, g in (("residual_out", ro), ("y", yo), ("q", qo), ("scale", so)):
+        if g is not None:
+            g.check()
+            out[name] = g.host()
+    if in_place:
+        out["residual_out"] = host_bits(R)
+    return out
+
+
+def check_fold(got, want, what):
+    if "residual_out" in want and want.get("residual_out") is not None and "residual_out" in got:
+        assert_bits_equal(got["residual_out"], want["residual_out"], f"{what} residual'")
+        assert_bf16_close(got["residual_out"], want["residual_out"], f"{what} residual'")
+    if "y" in got:
+        assert_bf16_close(got["y"], want["y"], f"{what} y")
+    if "q" in got:
+        assert_fp8_close(got["q"], want["q"], got["scale"], want["scale"], f"{what} fp8")
+
+
+# --------------------------------------------------------------------------------------
+# The specified workloads
+# --------------------------------------------------------------------------------------
+
+def test_tiny_fold_norm(lb):
+    w = wl.tiny_fold_norm()
+    want = oracle.fold_norm(w.partials, w.residual, w.gamma, w.eps)
+    check_fold(gpu_fold(lb, w.partials, w.residual, w.gamma, w.eps), want, "tiny")
+
+
+@pytest.mark.parametrize("initial", [False, True])
+def test_decode_fold_norm(lb, initial):
+    w = wl.decode_fold_norm(initial=initial)
+    assert (w.residual is None) == initial
+    want = oracle.fold_norm(w.partials, w.residual, w.gamma, w.eps)
+    check_fold(gpu_fold(lb, w.partials, w.residual, w.gamma, w.eps), want, w.name)
+
+
+def test_prefill_fold_norm_fp8_full_size(lb):
+    w = wl.prefill_fold_norm_fp8()
+    want = oracle.fold_norm(w.partials, w.residual, w.gamma, w.eps, want_fp8=True)
+    got = gpu_fold(lb, w.partials, w.residual, w.gamma, w.eps, fp8=True)
+    check_fold(got, want, "prefill fp8")
+    # outlier rows: residual' carries the x50 rows, the normalised read does not
+    big = np.abs((got["residual_out"].astype(np.uint32) << 16).view(np.float32)).max()
+    assert big > 50.0
+
+
+def test_prefill_fp8_with_bf16_read(lb):
+    w = wl.fold_workload("p", 4, 256, 4096, seed=2, outlier_frac=0.01, fp8=True)
+    want = oracle.fold_norm(w.partials, w.residual, w.gamma, w.eps, want_fp8=True)
+    got = gpu_fold(lb, w.partials, w.residual, w.gamma, w.eps, fp8=True, want_y_fp8=True)
+    check_fold(got, want, "fp8 + y")
+
+
+def _gpu_slice(lb, w, r, fp8=False):
+    S, H = w.T // 1, w.H
+    P = [dev_bits(p) for p in w.partials]
+    R = dev_bits(w.residual_full[r * S:(r + 1) * S])
+    G = torch.from_numpy(w.gamma).cuda()
+    ro, yo = Guarded(S, H, torch.bfloat16), Guarded(S, H, torch.bfloat16)
+    qo = Guarded(S, H, torch.uint8) if fp8 else None
+    so = Guarded(S, 0, torch.float32) if fp8 else None
+    before = _snapshot(P + [R, G])
+    lb.lb_slice_fold_norm(P, w.T_pad, w.num_slices, r, w.set_offsets, w.set_counts, R,
+                          ro.t, G, yo.t, qo.t if fp8 else None, so.t if fp8 else None, H,
+                          w.eps)
+    torch.cuda.synchronize()
+    _assert_unchanged(before, P + [R, G])
+    out = {"residual_out": ro, "y": yo}
+    if fp8:
+        out.update(q=qo, scale=so)
+    for g in out.values():
+        g.check()
+    return {k: g.host() for k, g in out.items()}
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_ragged_slice_every_rank(lb, fp8):
+    w = wl.ragged_slice()
+    S = w.T
+    assert (w.T_pad, S) == (2032, 254)
+    valid = np.zeros(w.T_pad, bool)
+    for o, c in zip(w.set_offsets, w.set_counts):
+        valid[o:o + c] = True
+    for r in range(w.num_slices):
+        sent = {"residual_out": np.full((S, w.H), SENTINEL16, np.uint16),
+                "y": np.full((S, w.H), SENTINEL16, np.uint16)}
+        want = oracle.slice_fold_norm(w.partials, w.T_pad, w.num_slices, r, w.set_offsets,
+                                      w.set_counts, w.residual_full[r * S:(r + 1) * S],
+                                      w.gamma, w.eps, want_fp8=fp8, out=sent)
+        got = _gpu_slice(lb, w, r, fp8=fp8)
+        v = valid[r * S:(r + 1) * S]
+        # placement: padding rows untouched, valid rows written -- bit-exact
+        assert_bits_equal(got["residual_out"][~v], want["residual_out"][~v], f"slice {r} pad")
+        assert np.all(got["y"][~v] == SENTINEL16)
+        assert_bits_equal(got["residual_out"], want["residual_out"], f"slice {r} residual'",
+                          rows=v)
+        assert_bf16_close(got["y"], want["y"], f"slice {r} y", rows=v)
+        if fp8:
+            assert np.all(got["q"][~v] == 0x7F)
+            assert_fp8_close(got["q"], want["q"], got["scale"], want["scale"],
+                             f"slice {r} fp8", rows=v)
+
+
+def _gpu_moe(lb, w, *, idx=None, residual=True, fp8=False, flag=False, want_y=True):
+    T, H = w.T, w.H
+    idx = w.idx if idx is None else idx
+    E = dev_bits(w.expert_out)
+    I = torch.from_numpy(np.ascontiguousarray(idx)).cuda()
+    Wt = torch.from_numpy(np.ascontiguousarray(w.w)).cuda()
+    R = dev_bits(w.residual) if residual else None
+    G = torch.from_numpy(w.gamma).cuda()
+    ro = Guarded(T, H, torch.bfloat16)
+    yo = Guarded(T, H, torch.bfloat16) if want_y else None
+    qo = Guarded(T, H, torch.uint8) if fp8 else None
+    so = Guarded(T, 0, torch.float32) if fp8 else None
+    F = torch.zeros(1, dtype=torch.int32, device="cuda") if flag else None
+    before = _snapshot([E, I, Wt, R, G])
+    lb.lb_moe_finalize_fold_norm(E, w.expert_out.shape[0], I, Wt, idx.shape[1], R, ro.t, G,
+                                 yo.t if yo else None, qo.t if fp8 else None,
+                                 so.t if fp8 else None, T, H, w.eps, F)
+    torch.cuda.synchronize()
+    _assert_unchanged(before, [E, I, Wt, R, G])
+    out = {"residual_out": ro}
+    if want_y:
+        out["y"] = yo
+    if fp8:
+        out.update(q=qo, scale=so)
+    for g in out.values():
+        g.check()
+    res = {k: g.host() for k, g in out.items()}
+    if flag:
+        res["flag"] = int(F.item())
+    return res
+
+
+def test_moe_finalize_full_size(lb):
+    w = wl.moe_finalize()
+    want = oracle.moe_finalize_fold_norm(w.expert_out, w.idx, w.w, w.residual, w.gamma, w.eps)
+    got = _gpu_moe(lb, w)
+    check_fold(got, want, "moe")
+
+
+def test_moe_finalize_fp8_and_initial(lb):
+    w = wl.moe_workload("m", 200, 2048, 32, 6, seed=41)
+    want = oracle.moe_finalize_fold_norm(w.expert_out, w.idx, w.w, None, w.gamma, w.eps,
+                                         want_fp8=True)
+    got = _gpu_moe(lb, w, residual=False, fp8=True)
+    check_fold(got, want, "moe fp8 initial")
+
+
+@pytest.mark.parametrize("T,H,E,topk", [(1, 4096, 16, 16), (37, 520, 8, 3), (64, 8192, 64, 8),
+                                        (5, 16384, 8, 1)])
+def test_moe_shapes(lb, T, H, E, topk):
+    w = wl.moe_workload("m", T, H, E, topk, seed=T + H)
+    want = oracle.moe_finalize_fold_norm(w.expert_out, w.idx, w.w, w.residual, w.gamma, w.eps)
+    check_fold(_gpu_moe(lb, w), want, f"moe {T}x{H} top{topk}")
+
+
+def test_moe_bad_index_is_skipped_and_flagged(lb):
+    w = wl.moe_workload("bad", 16, 256, 4, 4, seed=42)
+    idx = w.idx.copy()
+    idx[3, 2] = w.expert_out.shape[0]
+    idx[9, 0] = -5
+    want = oracle.moe_finalize_fold_norm(w.expert_out, idx, w.w, w.residual, w.gamma, w.eps)
+    assert want["bad_index"]
+    got = _gpu_moe(lb, w, idx=idx, flag=True)
+    assert got["flag"] == 1
+    check_fold(got, want, "moe bad index")
+    clean = _gpu_moe(lb, w, flag=True)
+    assert clean["flag"] == 0
+
+
+# --------------------------------------------------------------------------------------
+# Stream modes ("Residual stream" state table)
+# --------------------------------------------------------------------------------------
+
+def test_stream_modes(lb):
+    w = wl.fold_workload("modes", 3, 50, 1024, seed=51)
+    full = oracle.fold_norm(w.partials, w.residual, w.gamma, w.eps)
+    # enter (Initial): no residual
+    init = oracle.fold_norm(w.partials, None, w.gamma, w.eps)
+    check_fold(gpu_fold(lb, w.partials, None, w.gamma, w.eps), init, "enter")
+    # complete_output: the sum alone, no read
+    got = gpu_fold(lb, w.partials, None, w.gamma, w.eps, want_y=False)
+    assert set(got) == {"residual_out"}
+    assert_bits_equal(got["residual_out"], init["residual_out"], "complete_output")
+    # fold: residual updated, no read
+    got = gpu_fold(lb, w.partials, w.residual, w.gamma, w.eps, want_y=False)
+    assert_bits_equal(got["residual_out"], full["residual_out"], "fold")
+    # read of a Written stream: K = 0, no residual output
+    rd = oracle.fold_norm([], full["residual_out"], w.gamma, w.eps, want_residual=False)
+    got = gpu_fold(lb, [], full["residual_out"], w.gamma, w.eps, want_res=False)
+    assert set(got) == {"y"}
+    assert_bf16_close(got["y"], rd["y"], "read")
+    # fold + read in place (residual_out == residual_in)
+    got = gpu_fold(lb, w.partials, w.residual, w.gamma, w.eps, in_place=True)
+    check_fold(got, full, "in place")
+
+
+# --------------------------------------------------------------------------------------
+# Launch shapes and edge cases
+# --------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("K,T,H", [
+    (1, 1, 8),          # a single vector per row
+    (3, 5, 520),        # 65 vectors: partly active warp
+    (16, 3, 4096),      # maximum K; 8-CTA clusters
+    (2, 33, 8192),      # two vectors per thread, cluster split
+    (2, 400, 8192),     # two vectors per thread, no cluster
+    (2, 9, 16384),      # four vectors per thread
+    (1, 4, 32768),      # four vectors per thread, two-CTA clusters
+    (5, 301, 4096),     # K above one load chunk, ragged last wave
+    (4, 2048, 1024),
+    (8, 152, 2048),
+])
+def test_shapes(lb, K, T, H):
+    w = wl.fold_workload("shape", K, T, H, seed=K * 1000 + T + H)
+    want = oracle.fold_norm(w.partials, w.residual, w.gamma, w.eps, want_fp8=True)
+    check_fold(gpu_fold(lb, w.partials, w.residual, w.gamma, w.eps), want, f"{K}x{T}x{H}")
+    check_fold(gpu_fold(lb, w.partials, w.residual, w.gamma, w.eps, fp8=True,
+                        want_y_fp8=True), want, f"fp8 {K}x{T}x{H}")
+
+
+def test_empty_batch_writes_nothing(lb):
+    H = 256
+    P = [torch.zeros((1, H), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    ro, yo = Guarded(0, H, torch.bfloat16), Guarded(0, H, torch.bfloat16)
+    G = torch.ones(H, device="cuda")
+    lb.lb_fold_norm(P, P[0], ro.t, G, yo.t, 0, H, 1e-6)
+    torch.cuda.synchronize()
+    ro.check(), yo.check()
+
+
+def test_zero_rows_fp8(lb):
+    w = wl.fold_workload("z", 2, 8, 512, seed=61)
+    for a in w.partials + [w.residual]:
+        a[[1, 5]] = 0
+    want = oracle.fold_norm(w.partials, w.residual, w.gamma, w.eps, want_fp8=True)
+    assert want["scale"][1] == 0 and want["scale"][5] == 0
+    got = gpu_fold(lb, w.partials, w.residual, w.gamma, w.eps, fp8=True)
+    check_fold(got, want, "zero rows")
+    assert np.all(got["q"][[1, 5]] == 0) and np.all(got["scale"][[1, 5]] == 0)
+
+
+def test_repeat_calls_are_bit_identical(lb):
+    w = wl.fold_workload("rep", 4, 100, 4096, seed=71, fp8=True)
+    a = gpu_fold(lb, w.partials, w.residual, w.gamma, w.eps, fp8=True, want_y_fp8=True)
+    b = gpu_fold(lb, w.partials, w.residual, w.gamma, w.eps, fp8=True, want_y_fp8=True)
+    for k in a:
+        assert np.array_equal(a[k], b[k])
+
+
+def test_runs_on_a_side_stream(lb):
+    w = wl.fold_workload("stream", 2, 64, 2048, seed=72)
+    want = oracle.fold_norm(w.partials, w.residual, w.gamma, w.eps)
+    P = [dev_bits(p) for p in w.partials]
+    R = dev_bits(w.residual)
+    G = torch.from_numpy(w.gamma).cuda()
+    s = torch.cuda.Stream()
+    ro = torch.empty_like(R)
+    yo = torch.empty_like(R)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        lb.lb_fold_norm(P, R, ro, G, yo, 64, 2048, w.eps)
+    s.synchronize()
+    assert_bits_equal(host_bits(ro), want["residual_out"], "side stream residual'")
+    assert_bf16_close(host_bits(yo), want["y"], "side stream y")
