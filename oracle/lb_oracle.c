@@ -36,8 +36,11 @@
  *   round-to-nearest-even and saturation, scale = max|yf| / 448 over the FP32 yf;
  *   an all-zero row gets scale 0 and all codes 0x00.
  *
- * Arithmetic: IEEE binary32 throughout, every operation written separately; build
- * with -ffp-contract=off -fno-fast-math so that no multiply-add is contracted.
+ * Arithmetic: IEEE binary32 for the owed sum, the residual fold and the normalised
+ * output (the fused read keeps FP32 accumulation); the RMSNorm's sum of squares and
+ * its scalar 1/sqrt are taken in binary64 and rounded once, since the pages leave
+ * their precision open.  Every operation is written separately; build with
+ * -ffp-contract=off -fno-fast-math so that no multiply-add is contracted.
  *
  * Parity status: every function below is pinned by the CPU tests (hand-computed
  * cases, closed forms, invariants, library cross-checks); none is unpinned.
@@ -131,20 +134,24 @@ uint8_t ora_f32_to_e4m3(float x)
 /* Per-row steps                                                                   */
 /* ------------------------------------------------------------------------------ */
 
-/* Consumer read: RMSNorm of the FP32 row o[0..H) with weight gamma, in FP32.
- *   ms = (sum_h o[h]^2) / H      (sum in h order)
- *   r  = 1 / sqrt(ms + eps)
- *   yf[h] = (o[h] * r) * gamma[h]                                                  */
+/* Consumer read: RMSNorm of the FP32 row o[0..H) with weight gamma.
+ *   ms = (sum_h o[h]^2) / H            binary64 (exact squares, h order)
+ *   r  = (float)(1 / sqrt(ms + eps))   binary64, rounded once to binary32
+ *   yf[h] = (o[h] * r) * gamma[h]      binary32
+ * The pages fix FP32 for the accumulated residual o, which is what is normalised;
+ * they say nothing about the precision of the norm's own sum of squares, so it is
+ * taken in binary64: a sequential binary32 sum over a long row would carry an error
+ * growing with H that belongs to no reading of the method. */
 static void rmsnorm_row(const float *o, const float *gamma, int64_t H, float eps,
                         float *yf)
 {
-    float ss = 0.0f;
+    double ss = 0.0;
     for (int64_t h = 0; h < H; ++h) {
-        float sq = o[h] * o[h];
+        double sq = (double)o[h] * (double)o[h];
         ss = ss + sq;
     }
-    float ms = ss / (float)H;
-    float r = 1.0f / sqrtf(ms + eps);
+    double ms = ss / (double)H;
+    float r = (float)(1.0 / sqrt(ms + (double)eps));
     for (int64_t h = 0; h < H; ++h) {
         float t = o[h] * r;
         yf[h] = t * gamma[h];
