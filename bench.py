@@ -211,6 +211,11 @@ def time_graph(launches, steps, warmup, stream, dist, sampler=None):
     return start.elapsed_time(end) / 1e3, (t0, t1)
 
 
+def plan_of(lb, rows, H, n_inputs, props):
+    smem = getattr(props, "shared_memory_per_block_optin", 232448)
+    return lb.lb_launch_plan(rows, H, n_inputs, props.multi_processor_count, smem).as_dict()
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     files = sorted(glob.glob(os.path.join(ROOT, "layer_boundary_fusion_gb300", "csrc", "*")))
@@ -291,7 +296,7 @@ def measure_variants(lb, dev, stream, dist, steps):
                      "frac_of_measured_hbm": round(nbytes / t / 1e9 / peak, 4),
                      "bytes_per_call": nbytes, "launch": shape, "l2": l2}
 
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    props = torch.cuda.get_device_properties(dev)
     # decode: K=8 T=64, with and without a residual; rotated and hot-L2
     for name, w in (("decode_fold_norm", wl.decode_fold_norm()),
                     ("decode_initial", wl.decode_fold_norm(initial=True))):
@@ -300,9 +305,11 @@ def measure_variants(lb, dev, stream, dist, steps):
         sets = fold_sets(w, dev, ns, False)
         ls = [fold_launcher(lb, s, w.T, w.H, w.eps, False, stream) for s in sets]
         el, _ = time_graph(ls, steps, 20, stream, dist)
-        record(name, w.T, nb, el, steps, lb.lb_launch_shape(w.T, w.H, sms), f"rotated {ns} sets")
+        record(name, w.T, nb, el, steps, plan_of(lb, w.T, w.H, w.K + (w.residual is not None), props),
+               f"rotated {ns} sets")
         el, _ = time_graph(ls[:1], steps, 20, stream, dist)
-        record(name + "_hot_l2", w.T, nb, el, steps, lb.lb_launch_shape(w.T, w.H, sms),
+        record(name + "_hot_l2", w.T, nb, el, steps,
+               plan_of(lb, w.T, w.H, w.K + (w.residual is not None), props),
                "hot: one buffer set, L2-resident")
         del sets, ls
     # ragged row slice r=3 of 8
@@ -324,7 +331,8 @@ def measure_variants(lb, dev, stream, dist, steps):
                                             w.set_offsets, w.set_counts, s[1], s[2], G, s[3],
                                             None, None, w.H, w.eps, stream=sp)) for s in sets]
     el, _ = time_graph(ls, steps, 20, stream, dist)
-    record("ragged_slice", v, nb, el, steps, lb.lb_launch_shape(S, w.H, sms), f"rotated {ns} sets")
+    record("ragged_slice", v, nb, el, steps, plan_of(lb, S, w.H, w.K + 1, props),
+           f"rotated {ns} sets")
     del sets, ls, P0
     # MoE finalize T=1024 top-8
     w = wl.moe_finalize()
@@ -340,7 +348,8 @@ def measure_variants(lb, dev, stream, dist, steps):
                                                    s[1], s[2], G, s[3], None, None, w.T, w.H,
                                                    w.eps, None, stream=sp)) for s in sets]
     el, _ = time_graph(ls, steps, 20, stream, dist)
-    record("moe_finalize", w.T, nb, el, steps, lb.lb_launch_shape(w.T, w.H, sms), f"rotated {ns} sets")
+    record("moe_finalize", w.T, nb, el, steps, plan_of(lb, w.T, w.H, w.topk + 1, props),
+           f"rotated {ns} sets")
     del sets, ls
     # tiny correctness configuration
     w = wl.tiny_fold_norm()
@@ -348,7 +357,7 @@ def measure_variants(lb, dev, stream, dist, steps):
     sets = fold_sets(w, dev, 1, False)
     ls = [fold_launcher(lb, sets[0], w.T, w.H, w.eps, False, stream)]
     el, _ = time_graph(ls, steps, 20, stream, dist)
-    record("tiny_fold_norm", w.T, nb, el, steps, lb.lb_launch_shape(w.T, w.H, sms),
+    record("tiny_fold_norm", w.T, nb, el, steps, plan_of(lb, w.T, w.H, w.K + 1, props),
            "hot: one buffer set, L2-resident")
     torch.cuda.empty_cache()
     return out
@@ -448,7 +457,6 @@ def run_native(args, dist):
     variants = measure_variants(lb, dev, stream, dist, args.variant_steps)
     cpu = cpu_baseline(w) if (dist.rank == 0 and dist.world == 1) else None
 
-    sms = props.multi_processor_count
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
         "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
@@ -462,8 +470,7 @@ def run_native(args, dist):
                    "l2": f"inputs larger than L2: {ns} rotating buffer sets of "
                          f"{nbytes / 1e6:.1f} MB ({ns * nbytes / 1e6:.0f} MB total, L2 "
                          f"{props.L2_cache_size / 1e6:.0f} MB)",
-                   "launch": dict(zip(("threads", "vectors_per_thread", "ctas_per_row"),
-                                      lb.lb_launch_shape(w.T, w.H, sms))),
+                   "launch": plan_of(lb, w.T, w.H, w.K + 1, props),
                    "timing": "CUDA graphs of up to 500 launches, CUDA events on the "
                              "launching stream",
                    "parallelism": f"replica per GPU x{dist.world} (rows independent)"},

@@ -37,6 +37,7 @@
  *    decisions": a candidate that declines must do so before touching its inputs).
  *  - Empty batch: zero rows returns LB_OK and launches nothing ("Enter and leave the
  *    layer stack": an empty batch still completes owed work and skips the norm).
+ *    Only the scalar arguments are checked then; buffer pointers may be NULL.
  */
 #ifndef LB_H
 #define LB_H
@@ -73,14 +74,43 @@ int lb_last_cuda_error(void);
 /* Library version: major * 10000 + minor * 100 + patch. */
 int lb_version(void);
 
+/* Kernels of the library (lb_plan.kernel). */
+#define LB_KERNEL_ROW 0     /* one CTA, or a cluster of up to 8 CTAs, per token row */
+#define LB_KERNEL_STREAM 1  /* persistent CTAs streaming rows through TMA stages */
+
+/* How a call of `rows` rows is launched. */
+typedef struct {
+    int kernel;             /* LB_KERNEL_ROW or LB_KERNEL_STREAM */
+    int grid;               /* CTAs launched */
+    int threads;            /* threads per CTA */
+    int vectors_per_thread; /* 16-byte vectors of a row per (consumer) thread */
+    int ctas_per_row;       /* row kernel: CTAs (cluster size) per row; else 1 */
+    int stages;             /* stream kernel: shared-memory stages; else 0 */
+    int smem_bytes;         /* stream kernel: dynamic shared memory per CTA; else 0 */
+} lb_plan;
+
 /*
- * Launch shape that the library uses for `rows` rows of width H on a GPU with
- * `num_sms` SMs: threads per CTA, 16-byte vectors per thread and CTAs per row (a
- * thread-block cluster splits a row when there are too few rows to fill the GPU).
- * Host-only; returns LB_ERR_UNSUPPORTED for an H no shape covers.
+ * The launch the library makes for `rows` rows of width H, each reading `n_inputs`
+ * input rows (K partials or topk expert rows, plus one if there is a residual), on a
+ * GPU with `num_sms` SMs and `smem_per_block` bytes of opt-in shared memory per CTA.
+ * Host-only, pure.  Calls with at least one row per SM stream through the
+ * persistent TMA kernel when a double-buffered stage fits; smaller calls use the
+ * row kernel, splitting each row over a cluster when the rows alone cannot fill the
+ * GPU.  Returns LB_ERR_UNSUPPORTED for an H that no launch covers.
  */
-lb_status lb_launch_shape(int64_t rows, int64_t H, int num_sms, int *threads,
-                          int *vectors_per_thread, int *ctas_per_row);
+lb_status lb_launch_plan(int64_t rows, int64_t H, int n_inputs, int num_sms,
+                         int smem_per_block, lb_plan *plan);
+
+/* Device-side error flags (lb_device_error). */
+#define LB_DEVICE_ERR_TIMEOUT 1u  /* a bounded wait in the stream kernel gave up */
+
+/*
+ * Synchronises the current device, then returns in *flags the OR of the device-side
+ * error flags raised by the library's kernels since they were last cleared, and
+ * clears them when `clear` is nonzero.  A set flag means that some call since then
+ * produced incomplete outputs.  Not for use during stream capture.
+ */
+lb_status lb_device_error(unsigned int *flags, int clear);
 
 /*
  * lb_fold_norm — complete K partial sums, fold into the residual, RMSNorm read.

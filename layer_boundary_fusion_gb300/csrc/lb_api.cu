@@ -6,6 +6,7 @@
 // point is documented in include/lb.h.
 #include <cmath>
 #include <cstdint>
+#include <atomic>
 #include <climits>
 #include <cstring>
 
@@ -80,28 +81,62 @@ lb_status check_tensor(const void *p) {
             return s_;                     \
     } while (0)
 
-int device_sm_count(int *out) {
+// Per-device SM count and opt-in shared memory per block, cached after first use.
+struct DeviceInfo {
+    int sms;
+    int smem_optin;
+};
+
+int device_info(DeviceInfo *out) {
+    static std::atomic<int> cached[64];
+    static DeviceInfo info[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return static_cast<int>(e);
+    if (dev >= 0 && dev < 64 && cached[dev].load(std::memory_order_acquire)) {
+        *out = info[dev];
+        return 0;
+    }
+    DeviceInfo d{};
+    e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess)
-        e = cudaDeviceGetAttribute(out, cudaDevAttrMultiProcessorCount, dev);
-    return static_cast<int>(e);
+        e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess)
+        return static_cast<int>(e);
+    if (dev >= 0 && dev < 64) {
+        info[dev] = d;
+        cached[dev].store(1, std::memory_order_release);
+    }
+    *out = d;
+    return 0;
 }
 
-lb_status launch(const lb::Params &p, lb::Mode mode, bool fp8, cudaStream_t stream) {
-    int sms = 0;
-    const int e0 = device_sm_count(&sms);
+lb_status launch(const lb::Params &p, lb::Mode mode, bool fp8, int n_inputs,
+                 cudaStream_t stream) {
+    DeviceInfo d;
+    const int e0 = device_info(&d);
     if (e0 != 0) {
         g_last_cuda_error = e0;
         return LB_ERR_CUDA;
     }
-    lb::Shape s;
-    if (!lb::choose_shape(p.rows, p.H, sms, &s))
-        return LB_ERR_UNSUPPORTED;
     lb::Params q = p;
-    q.vec_per_cta = static_cast<int>(((p.H / 8) + s.ctas_per_row - 1) / s.ctas_per_row);
-    const cudaError_t e = (mode == lb::kFold) ? lb::launch_fold(q, s, fp8, stream)
-                                              : lb::launch_moe(q, s, fp8, stream);
+    q.inv_H = 1.0f / static_cast<float>(p.H);
+    cudaError_t e;
+    lb::StreamShape ss;
+    if (lb::use_stream_kernel(p.rows, d.sms) &&
+        lb::choose_stream_shape(p.rows, p.H, n_inputs, d.sms, d.smem_optin, &ss)) {
+        q.stages = ss.stages;
+        e = (mode == lb::kFold) ? lb::launch_fold_stream(q, ss, fp8, stream)
+                                : lb::launch_moe_stream(q, ss, fp8, stream);
+    } else {
+        lb::Shape s;
+        if (!lb::choose_shape(p.rows, p.H, d.sms, &s))
+            return LB_ERR_UNSUPPORTED;
+        q.vec_per_cta = static_cast<int>(((p.H / 8) + s.ctas_per_row - 1) / s.ctas_per_row);
+        e = (mode == lb::kFold) ? lb::launch_fold(q, s, fp8, stream)
+                                : lb::launch_moe(q, s, fp8, stream);
+    }
     if (e != cudaSuccess) {
         g_last_cuda_error = static_cast<int>(e);
         return LB_ERR_CUDA;
@@ -177,13 +212,17 @@ lb_status fold_common(const void *const *partials, int K, const void *residual_i
                       float *scale_out, int64_t T, int64_t H, float eps,
                       lb_stream_t stream) {
     LB_TRY(check_shape(T, H, eps));
+    if (K < 0)
+        return LB_ERR_INVALID_ARGUMENT;
+    if (K > LB_MAX_K)
+        return LB_ERR_UNSUPPORTED;
+    if (T == 0)
+        return LB_OK;                          // empty batch: no pointer is used
     BufList l;
     LB_TRY(check_fold_inputs(partials, K, T, residual_in, &l, H));
     LB_TRY(check_stream_buffers(residual_in, residual_out, gamma, y_out, q_out, scale_out, T,
                                 H, &l));
     LB_TRY(check_overlaps(l));
-    if (T == 0)
-        return LB_OK;
     lb::Params p;
     std::memset(&p, 0, sizeof p);
     for (int k = 0; k < K; ++k)
@@ -191,12 +230,45 @@ lb_status fold_common(const void *const *partials, int K, const void *residual_i
     p.K = K;
     set_stream_params(&p, residual_in, residual_out, gamma, y_out, q_out, scale_out, T, H,
                       eps);
-    return launch(p, lb::kFold, q_out != nullptr, reinterpret_cast<cudaStream_t>(stream));
+    return launch(p, lb::kFold, q_out != nullptr, K + (residual_in != nullptr ? 1 : 0),
+                  reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // namespace
 
 namespace lb {
+
+bool use_stream_kernel(int64_t rows, int num_sms) {
+    // Enough rows for one persistent CTA per SM; fewer rows go to the row kernel,
+    // which splits each row over a cluster to fill the GPU.
+    return rows >= num_sms;
+}
+
+bool choose_stream_shape(int64_t rows, int64_t H, int n_inputs, int num_sms,
+                         int smem_per_block, StreamShape *out) {
+    if (rows <= 0 || H <= 0 || H % 8 != 0 || n_inputs < 1 || n_inputs > LB_MAX_K + 1 ||
+        num_sms <= 0)
+        return false;
+    const int64_t nvec = H / 8;
+    const int ncw = static_cast<int>(nvec >= 256 ? 8 : (nvec + 31) / 32);
+    int64_t vpt = (nvec + ncw * 32 - 1) / (ncw * 32);
+    if (vpt > 4)
+        return false;
+    vpt = vpt <= 1 ? 1 : (vpt <= 2 ? 2 : 4);
+    const int64_t stage = static_cast<int64_t>(n_inputs) * H * 2;
+    const int64_t reserve = 1024;              // static shared memory and mbarriers
+    int64_t ns = (static_cast<int64_t>(smem_per_block) - reserve) / (stage + 16);
+    if (ns > 8)
+        ns = 8;
+    if (ns < 2)
+        return false;
+    out->grid = static_cast<int>(rows < num_sms ? rows : num_sms);
+    out->consumer_warps = ncw;
+    out->vpt = static_cast<int>(vpt);
+    out->stages = static_cast<int>(ns);
+    out->smem_bytes = static_cast<int>(ns * stage + 16 * ns);
+    return true;
+}
 
 bool choose_shape(int64_t rows, int64_t H, int num_sms, Shape *out) {
     if (rows < 0 || H <= 0 || H % 8 != 0 || num_sms <= 0)
@@ -241,16 +313,48 @@ int lb_last_cuda_error(void) { return g_last_cuda_error; }
 
 int lb_version(void) { return 100; }
 
-lb_status lb_launch_shape(int64_t rows, int64_t H, int num_sms, int *threads,
-                          int *vectors_per_thread, int *ctas_per_row) {
-    if (threads == nullptr || vectors_per_thread == nullptr || ctas_per_row == nullptr)
+lb_status lb_launch_plan(int64_t rows, int64_t H, int n_inputs, int num_sms,
+                         int smem_per_block, lb_plan *plan) {
+    if (plan == nullptr || n_inputs < 1 || n_inputs > LB_MAX_K + 1)
         return LB_ERR_INVALID_ARGUMENT;
+    std::memset(plan, 0, sizeof *plan);
+    lb::StreamShape ss;
+    if (lb::use_stream_kernel(rows, num_sms) &&
+        lb::choose_stream_shape(rows, H, n_inputs, num_sms, smem_per_block, &ss)) {
+        plan->kernel = LB_KERNEL_STREAM;
+        plan->grid = ss.grid;
+        plan->threads = 32 * (1 + ss.consumer_warps);
+        plan->vectors_per_thread = ss.vpt;
+        plan->ctas_per_row = 1;
+        plan->stages = ss.stages;
+        plan->smem_bytes = ss.smem_bytes;
+        return LB_OK;
+    }
     lb::Shape s;
     if (!lb::choose_shape(rows, H, num_sms, &s))
         return LB_ERR_UNSUPPORTED;
-    *threads = s.threads;
-    *vectors_per_thread = s.vpt;
-    *ctas_per_row = s.ctas_per_row;
+    plan->kernel = LB_KERNEL_ROW;
+    plan->grid = static_cast<int>(rows * s.ctas_per_row);
+    plan->threads = s.threads;
+    plan->vectors_per_thread = s.vpt;
+    plan->ctas_per_row = s.ctas_per_row;
+    return LB_OK;
+}
+
+lb_status lb_device_error(unsigned int *flags, int clear) {
+    if (flags == nullptr)
+        return LB_ERR_INVALID_ARGUMENT;
+    cudaError_t e = cudaDeviceSynchronize();
+    unsigned int a = 0, b = 0;
+    if (e == cudaSuccess)
+        e = lb::fold_device_error(&a, clear != 0);
+    if (e == cudaSuccess)
+        e = lb::moe_device_error(&b, clear != 0);
+    if (e != cudaSuccess) {
+        g_last_cuda_error = static_cast<int>(e);
+        return LB_ERR_CUDA;
+    }
+    *flags = a | b;
     return LB_OK;
 }
 
@@ -282,6 +386,8 @@ lb_status lb_moe_finalize_fold_norm(const void *expert_out, int64_t n_expert_row
         return LB_ERR_INVALID_ARGUMENT;
     if (topk > LB_MAX_TOPK || n_expert_rows > (int64_t(1) << 31))
         return LB_ERR_UNSUPPORTED;
+    if (T == 0)
+        return LB_OK;                          // empty batch: no pointer is used
     if (expert_out == nullptr || idx == nullptr || w == nullptr)
         return LB_ERR_INVALID_ARGUMENT;
     LB_TRY(check_tensor(expert_out));
@@ -296,8 +402,6 @@ lb_status lb_moe_finalize_fold_norm(const void *expert_out, int64_t n_expert_row
     LB_TRY(check_stream_buffers(residual_in, residual_out, gamma, y_out, q_out, scale_out, T,
                                 H, &l));
     LB_TRY(check_overlaps(l));
-    if (T == 0)
-        return LB_OK;
     lb::Params p;
     std::memset(&p, 0, sizeof p);
     p.expert_out = static_cast<const uint16_t *>(expert_out);
@@ -308,7 +412,8 @@ lb_status lb_moe_finalize_fold_norm(const void *expert_out, int64_t n_expert_row
     p.bad_index = bad_index_flag;
     set_stream_params(&p, residual_in, residual_out, gamma, y_out, q_out, scale_out, T, H,
                       eps);
-    return launch(p, lb::kMoe, q_out != nullptr, reinterpret_cast<cudaStream_t>(stream));
+    return launch(p, lb::kMoe, q_out != nullptr, topk + (residual_in != nullptr ? 1 : 0),
+                  reinterpret_cast<cudaStream_t>(stream));
 }
 
 lb_status lb_slice_fold_norm(const void *const *partials, int K, int64_t T_pad,
@@ -333,13 +438,17 @@ lb_status lb_slice_fold_norm(const void *const *partials, int K, int64_t T_pad,
     }
     const int64_t S = T_pad / num_slices;
     LB_TRY(check_shape(S, H, eps));
+    if (K < 0)
+        return LB_ERR_INVALID_ARGUMENT;
+    if (K > LB_MAX_K)
+        return LB_ERR_UNSUPPORTED;
+    if (S == 0)
+        return LB_OK;                          // empty batch: no pointer is used
     BufList l;
     LB_TRY(check_fold_inputs(partials, K, T_pad, residual_in, &l, H));
     LB_TRY(check_stream_buffers(residual_in, residual_out, gamma, y_out, q_out, scale_out, S,
                                 H, &l));
     LB_TRY(check_overlaps(l));
-    if (S == 0)
-        return LB_OK;
     lb::Params p;
     std::memset(&p, 0, sizeof p);
     for (int k = 0; k < K; ++k)
@@ -358,7 +467,8 @@ lb_status lb_slice_fold_norm(const void *const *partials, int K, int64_t T_pad,
         return LB_OK;                          // the slice holds padding only
     set_stream_params(&p, residual_in, residual_out, gamma, y_out, q_out, scale_out, S, H,
                       eps);
-    return launch(p, lb::kFold, q_out != nullptr, reinterpret_cast<cudaStream_t>(stream));
+    return launch(p, lb::kFold, q_out != nullptr, K + (residual_in != nullptr ? 1 : 0),
+                  reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

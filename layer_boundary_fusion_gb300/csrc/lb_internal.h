@@ -40,21 +40,44 @@ struct Params {
     int num_sets;
     int32_t set_lo[LB_MAX_SETS];
     int32_t set_hi[LB_MAX_SETS];
-    // launch shape: 16-byte vectors of one row handled by one CTA
+    // row kernel: 16-byte vectors of one row handled by one CTA
     int vec_per_cta;
+    // stream kernel: shared-memory stages, and 1/H for the mean of squares
+    int stages;
+    float inv_H;
 };
 
+// Row kernel: one CTA (or a cluster of CTAs) per row.
 struct Shape {
     int threads;
     int vpt;           // vectors per thread (1, 2 or 4)
     int ctas_per_row;  // thread-block cluster size along the row (1..8)
 };
 
-// Pure host function: the launch shape for `rows` rows of width H.
-bool choose_shape(int64_t rows, int64_t H, int num_sms, Shape *out);
+// Stream kernel: persistent CTAs, one producer warp + consumer warps, TMA stages.
+struct StreamShape {
+    int grid;
+    int consumer_warps;  // 1..8
+    int vpt;             // vectors per consumer thread (1, 2 or 4)
+    int stages;          // 2..8
+    int smem_bytes;      // dynamic shared memory per CTA
+};
 
-// Kernel launchers (one per translation unit).  Return the CUDA launch status.
+// Pure host functions choosing the launch.  n_inputs = input rows read per output row.
+bool choose_shape(int64_t rows, int64_t H, int num_sms, Shape *out);
+bool choose_stream_shape(int64_t rows, int64_t H, int n_inputs, int num_sms,
+                         int smem_per_block, StreamShape *out);
+bool use_stream_kernel(int64_t rows, int num_sms);
+
+// Kernel launchers (one pair per translation unit).  Return the CUDA launch status.
 cudaError_t launch_fold(const Params &p, const Shape &s, bool fp8, cudaStream_t stream);
 cudaError_t launch_moe(const Params &p, const Shape &s, bool fp8, cudaStream_t stream);
+cudaError_t launch_fold_stream(const Params &p, const StreamShape &s, bool fp8,
+                               cudaStream_t stream);
+cudaError_t launch_moe_stream(const Params &p, const StreamShape &s, bool fp8,
+                              cudaStream_t stream);
+// Read (and optionally clear) the device error word of each translation unit.
+cudaError_t fold_device_error(unsigned int *out, bool clear);
+cudaError_t moe_device_error(unsigned int *out, bool clear);
 
 }  // namespace lb

@@ -1,0 +1,472 @@
+// Persistent, warp-specialised boundary kernel for sm_103a: TMA bulk copies stream
+// every input row of the boundary into a ring of shared-memory stages while the
+// consumer warps fold, reduce and store earlier rows.
+//
+//   warp 0 (producer): for each of this CTA's rows, wait until its stage is free,
+//     post the byte count on the stage's "full" mbarrier and issue one
+//     cp.async.bulk (global -> shared) per input row: the K partial rows (or the
+//     gathered expert rows of a MoE finalize) and the residual row.
+//   warps 1..W (consumers): wait on "full", fold the stage's rows in binary32 in the
+//     definition's order, hand the stage back ("empty" mbarrier, one arrive per
+//     warp), store residual', reduce sum(o^2) across the consumer warps (shuffles +
+//     one named barrier), and store the bf16 read or the FP8 codes and scale.
+//     gamma stays in registers for the whole kernel.
+//
+// Loads in flight per SM are bounded by the stages (up to ~200 KB), not by
+// registers, and the fixed per-row costs (two reductions, one rsqrt) are spread over
+// 8-32 elements per consumer thread.
+//
+// Every wait is bounded: after about a second without progress the waiting thread
+// records LB_DEVICE_ERR_TIMEOUT in the library's device error word, the CTA stops
+// taking rows, the producer waits (again bounded) for the copies it has in flight,
+// and the kernel returns.
+//
+// Sources: "Layer boundaries" (sglang developer guide), sections "Residual stream"
+// and "Residual update and input read"; "SGLang flashinfer_allreduce_fusion精读",
+// section forward.  The pipeline itself is this library's GB300 design.
+#pragma once
+
+#include "lb_kernel.cuh"
+
+namespace lb {
+
+// Device error word of this translation unit (bit flags: LB_DEVICE_ERR_*), read and
+// cleared through lb_device_error().  Each kernel translation unit has its own copy.
+static __device__ unsigned int g_device_error = 0;
+constexpr unsigned int kDeviceErrTimeout = 1u;
+
+// Host side: synchronise nothing, read and optionally clear this unit's word.
+static inline cudaError_t read_device_error(unsigned int *out, bool clear) {
+    cudaError_t e = cudaMemcpyFromSymbol(out, g_device_error, sizeof(unsigned int));
+    if (e == cudaSuccess && clear) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(unsigned int));
+    }
+    return e;
+}
+
+// ------------------------------------------------------------------------------------
+// mbarrier / bulk-copy primitives
+// ------------------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait for the phase with the given parity: at most 2^24 polls and about one
+// second.  `abort_flag` (shared) is polled too, so a waiter gives up early once
+// another warp of the CTA has given up.  Returns false on time-out or abort.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  const volatile int *abort_flag) {
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 0; it < (1u << 24); ++it) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if ((it & 255u) == 255u) {
+            if (abort_flag != nullptr && *abort_flag)
+                return false;
+            if (global_timer_ns() - t0 > 1000000000ull)
+                return false;
+        }
+    }
+    return false;
+}
+
+// One bulk copy global -> this CTA's shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                         uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void consumer_sync(int nthreads) {
+    asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
+// Barrier over the consumer warps that also ORs a predicate across them.
+__device__ __forceinline__ bool consumer_sync_or(bool pred, int nthreads) {
+    uint32_t out;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(out)
+        : "r"(static_cast<uint32_t>(pred)), "r"(nthreads)
+        : "memory");
+    return out != 0;
+}
+
+// ------------------------------------------------------------------------------------
+// Row schedule shared by producer and consumers
+// ------------------------------------------------------------------------------------
+
+__device__ __forceinline__ bool row_valid(const Params &p, int64_t row) {
+    if (p.num_sets == 0)
+        return true;
+    const int64_t g = p.in_row0 + row;
+    bool v = false;
+    for (int s = 0; s < p.num_sets; ++s)
+        v |= (g >= p.set_lo[s]) & (g < p.set_hi[s]);
+    return v;
+}
+
+// Next valid row of this CTA at or after `row` (rows are dealt round-robin).
+__device__ __forceinline__ int64_t next_row(const Params &p, int64_t row) {
+    while (row < p.rows && !row_valid(p, row))
+        row += gridDim.x;
+    return row;
+}
+
+// ------------------------------------------------------------------------------------
+// The kernel
+// ------------------------------------------------------------------------------------
+
+// Shared-memory layout (dynamic): [stages][slot][slot_bytes] then the mbarriers.
+// Slot j < n_main holds partial j (fold) or routed row j (MoE); the residual row, if
+// any, is slot n_main.
+template <int kMode, bool kFp8, int kVpt>
+__global__ void __launch_bounds__(288, 1) stream_kernel(const __grid_constant__ Params p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ float red_ss[2][8];
+    __shared__ float red_mx[2][8];
+    __shared__ int abort_flag;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int ncw = (blockDim.x >> 5) - 1;               // consumer warps
+    const int ncthreads = ncw * 32;
+    const int ns = p.stages;
+    const bool has_res = p.residual_in != nullptr;
+    const int n_main = (kMode == kFold) ? p.K : p.topk;
+    const int n_slots = n_main + (has_res ? 1 : 0);
+    const uint32_t slot_bytes = static_cast<uint32_t>(p.H * 2);
+    const uint32_t stage_bytes = slot_bytes * n_slots;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + static_cast<size_t>(ns) * stage_bytes);
+    const uint32_t full0 = smem_addr(bars);
+    const uint32_t empty0 = smem_addr(bars + ns);
+    const uint32_t stage0 = smem_addr(smem);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < ns; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, ncw);
+        }
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        // ------------------------------ producer ------------------------------
+        int issued = 0;
+        bool ok = true;
+        for (int64_t row = next_row(p, blockIdx.x); row < p.rows;
+             row = next_row(p, row + gridDim.x), ++issued) {
+            const int s = issued % ns;
+            const uint32_t k = static_cast<uint32_t>(issued / ns);
+            bool free_ok = true;
+            if (k > 0 && lane == 0)
+                free_ok = mbar_wait_bounded(empty0 + 8 * s, (k - 1) & 1u, &abort_flag);
+            if (!__shfl_sync(0xFFFFFFFFu, free_ok, 0)) {
+                ok = false;
+                break;
+            }
+            // sources of this row: lane j handles slot j (n_slots <= 17 <= 32)
+            const void *src = nullptr;
+            if (lane < n_main) {
+                if (kMode == kFold) {
+                    src = p.partials[lane] + (p.in_row0 + row) * p.H;
+                } else {
+                    const int32_t e = __ldg(p.idx + row * p.topk + lane);
+                    if (e >= 0 && static_cast<int64_t>(e) < p.n_expert_rows)
+                        src = p.expert_out + static_cast<int64_t>(e) * p.H;
+                }
+            } else if (lane == n_main && has_res) {
+                src = p.residual_in + row * p.H;
+            }
+            const unsigned valid = __ballot_sync(0xFFFFFFFFu, src != nullptr);
+            const uint32_t full = full0 + 8 * s;
+            if (lane == 0)
+                mbar_arrive_expect_tx(full, slot_bytes * __popc(valid));
+            for (int j = 0; j < n_slots; ++j) {
+                const void *sj = reinterpret_cast<const void *>(
+                    __shfl_sync(0xFFFFFFFFu, reinterpret_cast<unsigned long long>(src), j));
+                if (lane == 0 && sj != nullptr)
+                    bulk_g2s(stage0 + s * stage_bytes + j * slot_bytes, sj, slot_bytes, full);
+            }
+        }
+        if (!ok) {
+            if (lane == 0) {
+                atomicOr(&g_device_error, kDeviceErrTimeout);
+                abort_flag = 1;
+            }
+        }
+        // Drain: the copies of the last stages issued must land before the CTA ends.
+        if (lane == 0) {
+            const int first = issued > ns ? issued - ns : 0;
+            for (int i = first; i < issued; ++i)
+                if (!mbar_wait_bounded(full0 + 8 * (i % ns), (i / ns) & 1u, nullptr))
+                    atomicOr(&g_device_error, kDeviceErrTimeout);
+        }
+        return;
+    }
+
+    // -------------------------------- consumers --------------------------------
+    const int ct = threadIdx.x - 32;
+    const int64_t nvec = p.H >> 3;
+    int64_t col[kVpt];
+    bool act[kVpt];
+    float gm[kVpt][8];
+#pragma unroll
+    for (int i = 0; i < kVpt; ++i) {
+        const int64_t v = ct + static_cast<int64_t>(i) * ncthreads;
+        act[i] = v < nvec;
+        col[i] = v * 8;
+        if (act[i] && (kFp8 || p.y_out != nullptr))
+            ld_gamma8(p.gamma + col[i], gm[i]);
+        else
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                gm[i][e] = 0.0f;
+    }
+    const bool need_read = kFp8 || p.y_out != nullptr;
+    const int cw = warp - 1;
+
+    int used = 0;
+    for (int64_t row = next_row(p, blockIdx.x); row < p.rows;
+         row = next_row(p, row + gridDim.x), ++used) {
+        const int s = used % ns;
+        const uint32_t k = static_cast<uint32_t>(used / ns);
+        const int par = used & 1;
+
+        // MoE: routing weights and index validity of this row (broadcast loads,
+        // issued before the wait so that their latency hides behind it)
+        float wj[kMode == kMoe ? LB_MAX_TOPK : 1];
+        bool okj[kMode == kMoe ? LB_MAX_TOPK : 1];
+        if (kMode == kMoe) {
+#pragma unroll
+            for (int j = 0; j < LB_MAX_TOPK; ++j) {
+                okj[j] = false;
+                wj[j] = 0.0f;
+                if (j < p.topk) {
+                    const int32_t e = __ldg(p.idx + row * p.topk + j);
+                    okj[j] = (e >= 0) & (static_cast<int64_t>(e) < p.n_expert_rows);
+                    wj[j] = __ldg(p.w + row * p.topk + j);
+                }
+            }
+            if (p.bad_index != nullptr && ct == 0) {
+                bool bad = false;
+#pragma unroll
+                for (int j = 0; j < LB_MAX_TOPK; ++j)
+                    bad |= (j < p.topk) & !okj[j];
+                if (bad)
+                    *p.bad_index = 1;
+            }
+        }
+
+        const bool ok = mbar_wait_bounded(full0 + 8 * s, k & 1u, &abort_flag);
+        __syncwarp();
+        if (consumer_sync_or(!ok, ncthreads)) {
+            if (ct == 0) {
+                atomicOr(&g_device_error, kDeviceErrTimeout);
+                abort_flag = 1;
+            }
+            return;
+        }
+
+        const uint8_t *stage = smem + static_cast<size_t>(s) * stage_bytes;
+        float acc[kVpt][8];
+#pragma unroll
+        for (int i = 0; i < kVpt; ++i)
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                acc[i][e] = 0.0f;
+#pragma unroll
+        for (int j = 0; j < LB_MAX_K; ++j) {
+            if (j >= n_main)
+                break;
+            if (kMode == kMoe && !okj[j])
+                continue;
+            const uint8_t *slot = stage + static_cast<size_t>(j) * slot_bytes;
+#pragma unroll
+            for (int i = 0; i < kVpt; ++i)
+                if (act[i]) {
+                    float f[8];
+                    unpack8(*reinterpret_cast<const uint4 *>(slot + col[i] * 2), f);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        acc[i][e] = (kMode == kMoe)
+                                        ? __fadd_rn(acc[i][e], __fmul_rn(wj[j], f[e]))
+                                        : __fadd_rn(acc[i][e], f[e]);
+                }
+        }
+        if (has_res) {
+            const uint8_t *slot = stage + static_cast<size_t>(n_main) * slot_bytes;
+#pragma unroll
+            for (int i = 0; i < kVpt; ++i)
+                if (act[i]) {
+                    float f[8];
+                    unpack8(*reinterpret_cast<const uint4 *>(slot + col[i] * 2), f);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        acc[i][e] = __fadd_rn(acc[i][e], f[e]);
+                }
+        }
+        // the stage's data is in registers: hand it back to the producer
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(empty0 + 8 * s);
+
+        if (p.residual_out != nullptr) {
+#pragma unroll
+            for (int i = 0; i < kVpt; ++i)
+                if (act[i])
+                    *reinterpret_cast<uint4 *>(p.residual_out + row * p.H + col[i]) =
+                        pack8(acc[i]);
+        }
+        if (!need_read)
+            continue;
+
+        // r = 1/sqrt(mean(o^2) + eps)
+        float ss = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kVpt; ++i)
+            if (act[i])
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    ss = __fmaf_rn(acc[i][e], acc[i][e], ss);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            ss += __shfl_xor_sync(0xFFFFFFFFu, ss, off);
+        if (lane == 0)
+            red_ss[par][cw] = ss;
+        consumer_sync(ncthreads);
+        ss = red_ss[par][0];
+        for (int w = 1; w < ncw; ++w)
+            ss += red_ss[par][w];
+        const float r = rsqrtf(__fmaf_rn(ss, p.inv_H, p.eps));
+
+#pragma unroll
+        for (int i = 0; i < kVpt; ++i)
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                acc[i][e] = __fmul_rn(__fmul_rn(acc[i][e], r), gm[i][e]);
+
+        if (p.y_out != nullptr) {
+#pragma unroll
+            for (int i = 0; i < kVpt; ++i)
+                if (act[i])
+                    *reinterpret_cast<uint4 *>(p.y_out + row * p.H + col[i]) = pack8(acc[i]);
+        }
+        if (!kFp8)
+            continue;
+
+        float mx = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kVpt; ++i)
+            if (act[i])
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    mx = fmaxf(mx, fabsf(acc[i][e]));
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+        if (lane == 0)
+            red_mx[par][cw] = mx;
+        consumer_sync(ncthreads);
+        mx = red_mx[par][0];
+        for (int w = 1; w < ncw; ++w)
+            mx = fmaxf(mx, red_mx[par][w]);
+        const bool nonzero = mx > 0.0f;
+        const float inv = nonzero ? __fdividef(448.0f, mx) : 0.0f;
+        if (ct == 0)
+            p.scale_out[row] = mx / 448.0f;
+#pragma unroll
+        for (int i = 0; i < kVpt; ++i)
+            if (act[i]) {
+                float v[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    v[e] = nonzero ? __fmul_rn(acc[i][e], inv) : 0.0f;
+                const uint32_t lo = cvt_e4m3x2(v[0], v[1]) | (cvt_e4m3x2(v[2], v[3]) << 16);
+                const uint32_t hi = cvt_e4m3x2(v[4], v[5]) | (cvt_e4m3x2(v[6], v[7]) << 16);
+                *reinterpret_cast<uint2 *>(p.q_out + row * p.H + col[i]) = make_uint2(lo, hi);
+            }
+    }
+}
+
+// ------------------------------------------------------------------------------------
+// Host-side launch
+// ------------------------------------------------------------------------------------
+
+template <int kMode, bool kFp8, int kVpt>
+cudaError_t launch_stream_variant(const Params &p, const StreamShape &s, cudaStream_t stream) {
+    auto kern = stream_kernel<kMode, kFp8, kVpt>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         s.smem_bytes);
+    if (e != cudaSuccess)
+        return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(s.grid), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(32 * (1 + s.consumer_warps)), 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(s.smem_bytes);
+    cfg.stream = stream;
+    cfg.numAttrs = 0;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+template <int kMode>
+cudaError_t launch_stream_mode(const Params &p, const StreamShape &s, bool fp8,
+                               cudaStream_t stream) {
+    switch (s.vpt) {
+    case 1:
+        return fp8 ? launch_stream_variant<kMode, true, 1>(p, s, stream)
+                   : launch_stream_variant<kMode, false, 1>(p, s, stream);
+    case 2:
+        return fp8 ? launch_stream_variant<kMode, true, 2>(p, s, stream)
+                   : launch_stream_variant<kMode, false, 2>(p, s, stream);
+    case 4:
+        return fp8 ? launch_stream_variant<kMode, true, 4>(p, s, stream)
+                   : launch_stream_variant<kMode, false, 4>(p, s, stream);
+    default:
+        return cudaErrorInvalidConfiguration;
+    }
+}
+
+}  // namespace lb

@@ -26,9 +26,23 @@ LB_MAX_TOPK = 16
 LB_MAX_SETS = 64
 LB_MAX_H = 131072
 
-EXPORTED = ("lb_status_string", "lb_last_cuda_error", "lb_version", "lb_launch_shape",
-            "lb_fold_norm", "lb_fold_norm_fp8", "lb_moe_finalize_fold_norm",
-            "lb_slice_fold_norm")
+LB_KERNEL_ROW = 0
+LB_KERNEL_STREAM = 1
+LB_DEVICE_ERR_TIMEOUT = 1
+
+EXPORTED = ("lb_status_string", "lb_last_cuda_error", "lb_version", "lb_launch_plan",
+            "lb_device_error", "lb_fold_norm", "lb_fold_norm_fp8",
+            "lb_moe_finalize_fold_norm", "lb_slice_fold_norm")
+
+
+class Plan(ctypes.Structure):
+    """lb_plan: how the library launches a call."""
+    _fields_ = [("kernel", ctypes.c_int), ("grid", ctypes.c_int), ("threads", ctypes.c_int),
+                ("vectors_per_thread", ctypes.c_int), ("ctas_per_row", ctypes.c_int),
+                ("stages", ctypes.c_int), ("smem_bytes", ctypes.c_int)]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
 
 
 class LibraryMissing(RuntimeError):
@@ -69,9 +83,10 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.lb_last_cuda_error.restype = _int
     lib.lb_version.argtypes = []
     lib.lb_version.restype = _int
-    ip = ctypes.POINTER(_int)
-    lib.lb_launch_shape.argtypes = [_i64, _i64, _int, ip, ip, ip]
-    lib.lb_launch_shape.restype = _int
+    lib.lb_launch_plan.argtypes = [_i64, _i64, _int, _int, _int, ctypes.POINTER(Plan)]
+    lib.lb_launch_plan.restype = _int
+    lib.lb_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), _int]
+    lib.lb_device_error.restype = _int
     lib.lb_fold_norm.argtypes = [ctypes.POINTER(_vp), _int, _vp, _vp, _vp, _vp, _i64, _i64,
                                  _f32, _vp]
     lib.lb_fold_norm.restype = _int
@@ -128,12 +143,20 @@ def lb_version() -> int:
     return load().lb_version()
 
 
-def lb_launch_shape(rows: int, H: int, num_sms: int):
-    """(threads, vectors_per_thread, ctas_per_row) the library launches with."""
-    t, v, c = _int(), _int(), _int()
-    _check(load().lb_launch_shape(rows, H, num_sms, ctypes.byref(t), ctypes.byref(v),
-                                  ctypes.byref(c)), "lb_launch_shape")
-    return t.value, v.value, c.value
+def lb_launch_plan(rows: int, H: int, n_inputs: int, num_sms: int,
+                   smem_per_block: int) -> Plan:
+    """The launch the library makes for such a call (pure host function)."""
+    plan = Plan()
+    _check(load().lb_launch_plan(rows, H, n_inputs, num_sms, smem_per_block,
+                                 ctypes.byref(plan)), "lb_launch_plan")
+    return plan
+
+
+def lb_device_error(clear: bool = True) -> int:
+    """Synchronise the device; return (and clear) the kernels' device error flags."""
+    flags = ctypes.c_uint(0)
+    _check(load().lb_device_error(ctypes.byref(flags), int(clear)), "lb_device_error")
+    return flags.value
 
 
 def lb_fold_norm(partials, residual_in, residual_out, gamma, y_out, T, H, eps,

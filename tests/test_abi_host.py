@@ -62,36 +62,59 @@ def test_header_constants_match_binding(lib):
         assert int(m.group(1)) == getattr(lib, name)
 
 
-@pytest.mark.parametrize("rows,H,shape", [
-    (2048, 4096, (512, 1, 1)),      # prefill: one CTA per row
-    (1024, 4096, (512, 1, 1)),
-    (64, 4096, (64, 1, 8)),         # decode: an 8-CTA cluster per row
-    (254, 4096, (256, 1, 2)),       # one slice of a ragged batch
-    (1, 4096, (64, 1, 8)),
-    (16, 512, (64, 1, 1)),
-    (4096, 8192, (512, 2, 1)),
-    (4096, 16384, (512, 4, 1)),
-    (4096, 32768, (512, 4, 2)),
-    (4096, 520, (96, 1, 1)),        # 65 vectors: a partly active warp
-    (4096, 8, (32, 1, 1)),
+SMEM = 232448          # opt-in shared memory per CTA on GB300
+
+
+@pytest.mark.parametrize("rows,H,n_in,plan", [
+    # (kernel, grid, threads, vectors/thread, ctas/row, stages, smem)
+    (2048, 4096, 5, (1, 152, 288, 2, 1, 5, 204880)),    # prefill K=4 + residual: stream
+    (1024, 4096, 9, (1, 152, 288, 2, 1, 3, 221232)),    # MoE top-8 + residual: stream
+    (254, 4096, 9, (1, 152, 288, 2, 1, 3, 221232)),     # one ragged slice: stream
+    (64, 4096, 9, (0, 512, 64, 1, 8, 0, 0)),            # decode: 8-CTA clusters per row
+    (1, 4096, 2, (0, 8, 64, 1, 8, 0, 0)),
+    (16, 512, 3, (0, 16, 64, 1, 1, 0, 0)),              # tiny: one CTA per row
+    (4096, 8192, 5, (1, 152, 288, 4, 1, 2, 163872)),
+    (4096, 8192, 9, (0, 4096, 512, 2, 1, 0, 0)),        # no double-buffered stage fits
+    (4096, 16384, 3, (0, 4096, 512, 4, 1, 0, 0)),
+    (4096, 32768, 2, (0, 8192, 512, 4, 2, 0, 0)),
+    (4096, 520, 2, (1, 152, 128, 1, 1, 8, 16768)),      # 65 vectors: partly active warp
+    (4096, 8, 2, (1, 152, 64, 1, 1, 8, 384)),
 ])
-def test_launch_shape(lib, rows, H, shape):
-    assert lib.lb_launch_shape(rows, H, 152) == shape
+def test_launch_plan(lib, rows, H, n_in, plan):
+    p = lib.lb_launch_plan(rows, H, n_in, 152, SMEM)
+    got = (p.kernel, p.grid, p.threads, p.vectors_per_thread, p.ctas_per_row, p.stages,
+           p.smem_bytes)
+    assert got == plan
 
 
-def test_launch_shape_covers_every_row_vector(lib):
+def test_launch_plan_covers_every_row_vector(lib):
     for H in list(range(8, 4096, 8)) + [8192, 12288, 16384, 24576, 65536, 131072]:
         for rows in (1, 7, 64, 300, 5000):
-            t, v, c = lib.lb_launch_shape(rows, H, 152)
-            per_cta = -(-(H // 8) // c)
-            assert t % 32 == 0 and 32 <= t <= 512 and v in (1, 2, 4) and 1 <= c <= 8
-            assert t * v >= per_cta and c * per_cta >= H // 8
+            for n_in in (1, 2, 5, 9, 17):
+                p = lib.lb_launch_plan(rows, H, n_in, 152, SMEM)
+                nvec = H // 8
+                if p.kernel == lib.LB_KERNEL_ROW:
+                    per_cta = -(-nvec // p.ctas_per_row)
+                    assert p.threads % 32 == 0 and 32 <= p.threads <= 512
+                    assert p.threads * p.vectors_per_thread >= per_cta
+                    assert p.ctas_per_row * per_cta >= nvec and 1 <= p.ctas_per_row <= 8
+                    assert p.grid == rows * p.ctas_per_row
+                else:
+                    consumers = p.threads - 32
+                    assert consumers % 32 == 0 and 32 <= consumers <= 256
+                    assert consumers * p.vectors_per_thread >= nvec
+                    assert 2 <= p.stages <= 8 and p.grid == min(rows, 152)
+                    assert p.smem_bytes == p.stages * (n_in * H * 2 + 16)
+                    assert p.smem_bytes + 1024 <= SMEM
+                assert p.vectors_per_thread in (1, 2, 4)
 
 
-def test_launch_shape_rejects(lib):
-    for args in ((10, 12, 152), (10, 0, 152), (10, lib.LB_MAX_H + 8, 152), (10, 4096, 0)):
+def test_launch_plan_rejects(lib):
+    for args in ((10, 12, 2, 152, SMEM), (10, 0, 2, 152, SMEM),
+                 (10, lib.LB_MAX_H + 8, 2, 152, SMEM), (10, 4096, 2, 0, SMEM),
+                 (10, 4096, 0, 152, SMEM), (10, 4096, 18, 152, SMEM)):
         with pytest.raises(lib.LBError):
-            lib.lb_launch_shape(*args)
+            lib.lb_launch_plan(*args)
 
 
 _VALIDATION_SCRIPT = r"""
@@ -130,6 +153,9 @@ run("y_overlaps_partial", f, P, a(2), a(3), a(4), a(0) + 16, T, H, 1e-6, 0)
 run("y_overlaps_residual_out", f, P, a(2), a(3), a(4), a(3) + 16, T, H, 1e-6, 0)
 run("residual_out_shifted_over_in", f, P, a(2), a(2) + 16, a(4), a(5), T, H, 1e-6, 0)
 run("in_place_empty_ok", f, P, a(2), a(2), a(4), a(5), 0, H, 1e-6, 0)
+run("empty_null_buffers_ok", f, [], None, None, None, None, 0, H, 1e-6, 0)
+run("empty_bad_H", f, [], None, None, None, None, 0, 12, 1e-6, 0)
+run("empty_K_too_big", f, [None] * 17, None, None, None, None, 0, H, 1e-6, 0)
 g = lb.lb_fold_norm_fp8
 run("fp8_empty_ok", g, P, a(2), a(3), a(4), a(6), a(7), a(5), 0, H, 1e-6, 0)
 run("fp8_no_q", g, P, a(2), a(3), a(4), None, a(7), a(5), T, H, 1e-6, 0)
@@ -171,6 +197,7 @@ EXPECTED = {
     "T_negative": 1, "eps_negative": 1, "eps_nan": 1, "y_misaligned": 2,
     "gamma_misaligned": 2, "y_overlaps_partial": 1, "y_overlaps_residual_out": 1,
     "residual_out_shifted_over_in": 1, "in_place_empty_ok": 0,
+    "empty_null_buffers_ok": 0, "empty_bad_H": 3, "empty_K_too_big": 3,
     "fp8_empty_ok": 0, "fp8_no_q": 1, "fp8_no_scale": 1, "fp8_no_gamma": 1,
     "fp8_scale_misaligned": 2, "fp8_q_overlaps_y": 1,
     "moe_empty_ok": 0, "moe_topk0": 1, "moe_topk_big": 3, "moe_no_idx": 1, "moe_no_w": 1,

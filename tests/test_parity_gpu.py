@@ -27,7 +27,16 @@ def lb():
     from layer_boundary_fusion_gb300 import build, lb as binding
     build.build()
     binding.load()
-    return binding
+    binding.lb_device_error(clear=True)
+    yield binding
+    # no bounded wait of the stream kernel may have timed out in any test
+    assert binding.lb_device_error(clear=True) == 0
+
+
+def plan(lb, rows, H, n_in):
+    props = torch.cuda.get_device_properties(0)
+    return lb.lb_launch_plan(rows, H, n_in, props.multi_processor_count,
+                             props.shared_memory_per_block_optin)
 
 
 def _snapshot(ts):
@@ -259,6 +268,55 @@ def test_stream_modes(lb):
     # fold + read in place (residual_out == residual_in)
     got = gpu_fold(lb, w.partials, w.residual, w.gamma, w.eps, in_place=True)
     check_fold(got, full, "in place")
+
+
+@pytest.mark.parametrize("T", [50, 700])
+def test_stream_modes_on_both_kernels(lb, T):
+    """The same stream modes with enough rows for the persistent TMA kernel (T=700)
+    and few enough for the row kernel (T=50)."""
+    w = wl.fold_workload("modes2", 3, T, 2048, seed=52 + T)
+    kernel = lb.LB_KERNEL_STREAM if T >= torch.cuda.get_device_properties(0) \
+        .multi_processor_count else lb.LB_KERNEL_ROW
+    assert plan(lb, T, 2048, 4).kernel == kernel
+    full = oracle.fold_norm(w.partials, w.residual, w.gamma, w.eps, want_fp8=True)
+    init = oracle.fold_norm(w.partials, None, w.gamma, w.eps, want_fp8=True)
+    check_fold(gpu_fold(lb, w.partials, None, w.gamma, w.eps), init, "enter")
+    check_fold(gpu_fold(lb, w.partials, None, w.gamma, w.eps, fp8=True), init, "enter fp8")
+    got = gpu_fold(lb, w.partials, None, w.gamma, w.eps, want_y=False)
+    assert_bits_equal(got["residual_out"], init["residual_out"], "complete_output")
+    got = gpu_fold(lb, w.partials, w.residual, w.gamma, w.eps, want_y=False)
+    assert_bits_equal(got["residual_out"], full["residual_out"], "fold")
+    rd = oracle.fold_norm([], full["residual_out"], w.gamma, w.eps, want_residual=False,
+                          want_fp8=True)
+    check_fold(gpu_fold(lb, [], full["residual_out"], w.gamma, w.eps, want_res=False), rd,
+               "read")
+    check_fold(gpu_fold(lb, [], full["residual_out"], w.gamma, w.eps, want_res=False,
+                        fp8=True), rd, "read fp8")
+    check_fold(gpu_fold(lb, w.partials, w.residual, w.gamma, w.eps, in_place=True), full,
+               "in place")
+    check_fold(gpu_fold(lb, w.partials, w.residual, w.gamma, w.eps, in_place=True, fp8=True,
+                        want_y_fp8=True), full, "in place fp8")
+
+
+def test_moe_bad_index_on_the_stream_kernel(lb):
+    w = wl.moe_workload("bad2", 400, 1024, 16, 4, seed=43)
+    assert plan(lb, 400, 1024, 5).kernel == lb.LB_KERNEL_STREAM
+    idx = w.idx.copy()
+    idx[7, 1] = 1 << 30
+    idx[300, 3] = -1
+    idx[301, :] = -2                                   # a row with no valid expert
+    want = oracle.moe_finalize_fold_norm(w.expert_out, idx, w.w, w.residual, w.gamma, w.eps)
+    got = _gpu_moe(lb, w, idx=idx, flag=True)
+    assert got["flag"] == 1
+    check_fold(got, want, "moe bad index, stream kernel")
+
+
+def test_specified_workloads_take_the_intended_kernels(lb):
+    assert plan(lb, 2048, 4096, 5).kernel == lb.LB_KERNEL_STREAM     # prefill
+    assert plan(lb, 1024, 4096, 9).kernel == lb.LB_KERNEL_STREAM     # MoE finalize
+    assert plan(lb, 254, 4096, 9).kernel == lb.LB_KERNEL_STREAM      # ragged slice
+    p = plan(lb, 64, 4096, 9)                                        # decode
+    assert p.kernel == lb.LB_KERNEL_ROW and p.ctas_per_row > 1
 
 
 # --------------------------------------------------------------------------------------
