@@ -103,6 +103,7 @@ lb_status lb_launch_plan(int64_t rows, int64_t H, int n_inputs, int num_sms,
 
 /* Device-side error flags (lb_device_error). */
 #define LB_DEVICE_ERR_TIMEOUT 1u  /* a bounded wait in the stream kernel gave up */
+#define LB_DEVICE_ERR_LAUNCH 2u   /* the stream kernel refused an inconsistent launch */
 
 /*
  * Synchronises the current device, then returns in *flags the OR of the device-side

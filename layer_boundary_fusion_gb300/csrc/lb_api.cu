@@ -127,6 +127,8 @@ lb_status launch(const lb::Params &p, lb::Mode mode, bool fp8, int n_inputs,
     if (lb::use_stream_kernel(p.rows, d.sms) &&
         lb::choose_stream_shape(p.rows, p.H, n_inputs, d.sms, d.smem_optin, &ss)) {
         q.stages = ss.stages;
+        q.groups = ss.groups;
+        q.consumer_warps = ss.consumer_warps;
         e = (mode == lb::kFold) ? lb::launch_fold_stream(q, ss, fp8, stream)
                                 : lb::launch_moe_stream(q, ss, fp8, stream);
     } else {
@@ -250,19 +252,42 @@ bool choose_stream_shape(int64_t rows, int64_t H, int n_inputs, int num_sms,
         num_sms <= 0)
         return false;
     const int64_t nvec = H / 8;
-    const int ncw = static_cast<int>(nvec >= 256 ? 8 : (nvec + 31) / 32);
+    const int64_t maxw = LB_STREAM_CONSUMER_WARPS;
+    const int ncw = static_cast<int>(nvec >= 32 * maxw ? maxw : (nvec + 31) / 32);
     int64_t vpt = (nvec + ncw * 32 - 1) / (ncw * 32);
     if (vpt > 4)
         return false;
     vpt = vpt <= 1 ? 1 : (vpt <= 2 ? 2 : 4);
     const int64_t stage = static_cast<int64_t>(n_inputs) * H * 2;
     const int64_t reserve = 1024;              // static shared memory and mbarriers
-    int64_t ns = (static_cast<int64_t>(smem_per_block) - reserve) / (stage + 16);
-    if (ns > 8)
-        ns = 8;
+    int64_t per_cta = LB_SMEM_PER_SM / LB_STREAM_CTAS_PER_SM - 1024;
+    if (per_cta > smem_per_block)
+        per_cta = smem_per_block;
+    int64_t ns = (per_cta - reserve) / (stage + 16);
+    if (ns > LB_STREAM_MAX_STAGES)
+        ns = LB_STREAM_MAX_STAGES;
     if (ns < 2)
         return false;
-    out->grid = static_cast<int>(rows < num_sms ? rows : num_sms);
+    // Row i uses stage i % ns and consumer group i % groups.  The stage count is a
+    // multiple of the group count, so that every stage belongs to one group and its
+    // uses are consumed in order: a parity wait on an mbarrier tells only two
+    // consecutive phases apart.
+    int64_t groups = vpt >= 4 ? 1 : LB_STREAM_GROUPS;
+    if (groups > ns)
+        groups = ns;
+    ns -= ns % groups;
+    const int64_t ctas = static_cast<int64_t>(num_sms) * LB_STREAM_CTAS_PER_SM;
+    int64_t grid = rows < ctas ? rows : ctas;
+#ifdef LB_STREAM_BALANCED
+    // largest grid <= ctas that divides the rows evenly, if it keeps >= 3/4 of the SMs
+    for (int64_t g = grid; g * 4 >= ctas * 3; --g)
+        if (rows % g == 0) {
+            grid = g;
+            break;
+        }
+#endif
+    out->grid = static_cast<int>(grid);
+    out->groups = static_cast<int>(groups);
     out->consumer_warps = ncw;
     out->vpt = static_cast<int>(vpt);
     out->stages = static_cast<int>(ns);
@@ -323,7 +348,7 @@ lb_status lb_launch_plan(int64_t rows, int64_t H, int n_inputs, int num_sms,
         lb::choose_stream_shape(rows, H, n_inputs, num_sms, smem_per_block, &ss)) {
         plan->kernel = LB_KERNEL_STREAM;
         plan->grid = ss.grid;
-        plan->threads = 32 * (1 + ss.consumer_warps);
+        plan->threads = 32 * (1 + ss.groups * ss.consumer_warps);
         plan->vectors_per_thread = ss.vpt;
         plan->ctas_per_row = 1;
         plan->stages = ss.stages;

@@ -8,6 +8,26 @@
 
 #include "lb.h"
 
+// Stream-kernel launch parameters (compile-time, so that the kernel's register
+// budget matches the launch): persistent CTAs per SM, consumer warps per CTA, and the
+// largest number of shared-memory stages per CTA.
+#ifndef LB_STREAM_CTAS_PER_SM
+#define LB_STREAM_CTAS_PER_SM 1
+#endif
+#ifndef LB_STREAM_CONSUMER_WARPS
+#define LB_STREAM_CONSUMER_WARPS 8
+#endif
+#ifndef LB_STREAM_GROUPS
+#define LB_STREAM_GROUPS 2
+#endif
+#ifndef LB_STREAM_MAX_STAGES
+#define LB_STREAM_MAX_STAGES 8
+#endif
+// Shared memory of one SM (GB300: 228 KB), shared by the CTAs resident on it.
+#ifndef LB_SMEM_PER_SM
+#define LB_SMEM_PER_SM 233472
+#endif
+
 namespace lb {
 
 enum Mode : int { kFold = 0, kMoe = 1 };
@@ -42,8 +62,10 @@ struct Params {
     int32_t set_hi[LB_MAX_SETS];
     // row kernel: 16-byte vectors of one row handled by one CTA
     int vec_per_cta;
-    // stream kernel: shared-memory stages, and 1/H for the mean of squares
+    // stream kernel: shared-memory stages, consumer groups x warps, 1/H
     int stages;
+    int groups;
+    int consumer_warps;
     float inv_H;
 };
 
@@ -57,7 +79,8 @@ struct Shape {
 // Stream kernel: persistent CTAs, one producer warp + consumer warps, TMA stages.
 struct StreamShape {
     int grid;
-    int consumer_warps;  // 1..8
+    int groups;          // consumer groups, each folding its own rows
+    int consumer_warps;  // warps per group
     int vpt;             // vectors per consumer thread (1, 2 or 4)
     int stages;          // 2..8
     int smem_bytes;      // dynamic shared memory per CTA

@@ -16,7 +16,9 @@
 //      DSMEM across the cluster), r = 1/sqrt(ss/H + eps) with IEEE sqrt and divide;
 //   5. store y = bf16((o*r)*gamma) from registers, and for the FP8 read reduce
 //      max|yf| the same way and store E4M3 codes and the per-token scale.
-// Nothing is re-read and nothing is staged in global memory.
+// Nothing is re-read and nothing is staged in global memory.  Launches are
+// programmatic dependents of the previous kernel in the stream: the launch overlaps
+// its tail, and every global access waits for it (griddepcontrol.wait).
 //
 // Sources: "Layer boundaries" (sglang developer guide), sections "Residual stream"
 // and "Residual update and input read" (fused add+norm, FP32 accumulation);
@@ -58,6 +60,23 @@ __device__ __forceinline__ void ld_gamma8(const float *g, float out[8]) {
     const float4 b = __ldg(reinterpret_cast<const float4 *>(g) + 1);
     out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;
     out[4] = b.x; out[5] = b.y; out[6] = b.z; out[7] = b.w;
+}
+
+// ------------------------------------------------------------------------------------
+// Programmatic dependent launch
+// ------------------------------------------------------------------------------------
+
+// Lets the next kernel of the stream (if launched as a programmatic dependent) be
+// scheduled now, so that its launch and prologue overlap the rest of this kernel.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Waits until the kernels this one depends on have completed and their memory is
+// visible.  Every global memory access of a boundary kernel comes after this call,
+// so inputs produced by the previous kernel (a GEMM, the last boundary) are safe.
+__device__ __forceinline__ void pdl_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ------------------------------------------------------------------------------------
@@ -182,6 +201,8 @@ __global__ void __launch_bounds__(512, MinBlocks<kVpt>::value)
     __shared__ float cl_ss;
     __shared__ float cl_mx;
 
+    pdl_launch_dependents();
+    pdl_wait();
     const int cs = cluster_size();                 // 1 without a cluster launch
     const int crank = (cs > 1) ? cluster_rank() : 0;
     const int64_t row = blockIdx.x / cs;           // all CTAs of a cluster share it
@@ -406,14 +427,17 @@ cudaError_t launch_variant(const Params &p, const Shape &s, cudaStream_t stream)
     cfg.blockDim = dim3(static_cast<unsigned>(s.threads), 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (s.ctas_per_row > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = static_cast<unsigned>(s.ctas_per_row);
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = static_cast<unsigned>(s.ctas_per_row);
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
     }
     return cudaLaunchKernelEx(&cfg, boundary_kernel<kMode, kFp8, kVpt>, p);
 }

@@ -6,14 +6,15 @@
 //     post the byte count on the stage's "full" mbarrier and issue one
 //     cp.async.bulk (global -> shared) per input row: the K partial rows (or the
 //     gathered expert rows of a MoE finalize) and the residual row.
-//   warps 1..W (consumers): wait on "full", fold the stage's rows in binary32 in the
-//     definition's order, hand the stage back ("empty" mbarrier, one arrive per
-//     warp), store residual', reduce sum(o^2) across the consumer warps (shuffles +
-//     one named barrier), and store the bf16 read or the FP8 codes and scale.
-//     gamma stays in registers for the whole kernel.
+//   consumer groups of W warps (rows dealt to the groups in turn, so that several
+//     rows are reduced at once): wait on "full", fold the stage's rows in binary32 in
+//     the definition's order, hand the stage back ("empty" mbarrier, one arrive per
+//     warp), store residual', reduce sum(o^2) (and max|o*gamma| for FP8) across the
+//     group with shuffles and ONE named barrier per row, and store the bf16 read or
+//     the FP8 codes and scale.  gamma stays in registers for the whole kernel.
 //
 // Loads in flight per SM are bounded by the stages (up to ~200 KB), not by
-// registers, and the fixed per-row costs (two reductions, one rsqrt) are spread over
+// registers, and the fixed per-row costs (one barrier, one rsqrt) are spread over
 // 8-32 elements per consumer thread.
 //
 // Every wait is bounded: after about a second without progress the waiting thread
@@ -34,6 +35,7 @@ namespace lb {
 // cleared through lb_device_error().  Each kernel translation unit has its own copy.
 static __device__ unsigned int g_device_error = 0;
 constexpr unsigned int kDeviceErrTimeout = 1u;
+constexpr unsigned int kDeviceErrLaunch = 2u;
 
 // Host side: synchronise nothing, read and optionally clear this unit's word.
 static inline cudaError_t read_device_error(unsigned int *out, bool clear) {
@@ -114,24 +116,6 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         : "memory");
 }
 
-__device__ __forceinline__ void consumer_sync(int nthreads) {
-    asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
-}
-
-// Barrier over the consumer warps that also ORs a predicate across them.
-__device__ __forceinline__ bool consumer_sync_or(bool pred, int nthreads) {
-    uint32_t out;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, 1, %2, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(out)
-        : "r"(static_cast<uint32_t>(pred)), "r"(nthreads)
-        : "memory");
-    return out != 0;
-}
-
 // ------------------------------------------------------------------------------------
 // Row schedule shared by producer and consumers
 // ------------------------------------------------------------------------------------
@@ -157,20 +141,48 @@ __device__ __forceinline__ int64_t next_row(const Params &p, int64_t row) {
 // The kernel
 // ------------------------------------------------------------------------------------
 
+// Threads per CTA the kernel is compiled for: one producer warp plus the consumer
+// groups.  Four-vector threads need more registers and run one group.
+template <int kVpt>
+struct StreamThreads {
+    static constexpr int groups = (kVpt >= 4) ? 1 : LB_STREAM_GROUPS;
+    static constexpr int value = 32 * (1 + groups * LB_STREAM_CONSUMER_WARPS);
+};
+
+// Group-local barrier that also ORs a predicate over the group (barrier id 1 + g).
+__device__ __forceinline__ bool group_sync_or(bool pred, int id, int nthreads) {
+    uint32_t out;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(out)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+        : "memory");
+    return out != 0;
+}
+
 // Shared-memory layout (dynamic): [stages][slot][slot_bytes] then the mbarriers.
 // Slot j < n_main holds partial j (fold) or routed row j (MoE); the residual row, if
-// any, is slot n_main.
+// any, is slot n_main.  The CTA's rows are numbered i = 0, 1, ... in the order the
+// producer streams them; stage i % stages holds row i, and consumer group i % groups
+// processes it, so that `groups` rows are folded and reduced at the same time.
+// `stages` is a multiple of `groups`: stage s then belongs to group s % groups alone
+// and each stage's uses are waited for in order, which the one-bit phase parity of
+// an mbarrier wait requires (a group that skipped ahead to use k of a stage whose use
+// k-1 had not landed would see phase k-1's parity as complete).
 template <int kMode, bool kFp8, int kVpt>
-__global__ void __launch_bounds__(288, 1) stream_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
+    stream_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ float red_ss[2][8];
-    __shared__ float red_mx[2][8];
+    __shared__ float2 red[LB_STREAM_GROUPS][2][LB_STREAM_CONSUMER_WARPS];
     __shared__ int abort_flag;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int ncw = (blockDim.x >> 5) - 1;               // consumer warps
-    const int ncthreads = ncw * 32;
+    const int W = p.consumer_warps;                      // warps per consumer group
+    const int G = p.groups;
     const int ns = p.stages;
     const bool has_res = p.residual_in != nullptr;
     const int n_main = (kMode == kFold) ? p.K : p.topk;
@@ -182,22 +194,53 @@ __global__ void __launch_bounds__(288, 1) stream_kernel(const __grid_constant__ 
     const uint32_t empty0 = smem_addr(bars + ns);
     const uint32_t stage0 = smem_addr(smem);
 
+    if (G < 1 || ns % G != 0) {                           // launch contract, see above
+        if (threadIdx.x == 0)
+            atomicOr(&g_device_error, kDeviceErrLaunch);
+        return;
+    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < ns; ++s) {
             mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, ncw);
+            mbar_init(empty0 + 8 * s, W);
         }
         abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
+    // Each role reads its launch parameters before griddepcontrol.wait, so that their
+    // first (cache-missing) reads overlap the previous kernel; no global memory is
+    // touched before the wait.
+    pdl_launch_dependents();
 
     if (warp == 0) {
         // ------------------------------ producer ------------------------------
         int issued = 0;
         bool ok = true;
-        for (int64_t row = next_row(p, blockIdx.x); row < p.rows;
-             row = next_row(p, row + gridDim.x), ++issued) {
+        // Lane j's source base: partial j (fold), the residual (lane n_main), or the
+        // expert rows (MoE, row chosen per token below).
+        const uint16_t *lane_base = nullptr;
+        int64_t lane_row0 = 0;
+        if (kMode == kFold && lane < n_main) {
+            lane_base = p.partials[lane];
+            lane_row0 = p.in_row0;
+        } else if (lane == n_main && has_res) {
+            lane_base = p.residual_in;
+        }
+        const uint16_t *experts = p.expert_out;
+        const int64_t n_experts = p.n_expert_rows;
+        const int32_t *idx = p.idx;
+        const int topk = p.topk;
+        const int64_t H = p.H;
+        const int64_t rows = p.rows;
+        int64_t row = next_row(p, blockIdx.x);
+        pdl_wait();
+        // MoE: each lane < topk holds the expert row of its slot, loaded one row ahead
+        // so that the index latency hides behind the wait for a free stage.
+        int32_t e_next = -1;
+        if (kMode == kMoe && lane < n_main && row < rows)
+            e_next = __ldg(idx + row * topk + lane);
+        for (; row < rows; ++issued) {
             const int s = issued % ns;
             const uint32_t k = static_cast<uint32_t>(issued / ns);
             bool free_ok = true;
@@ -209,16 +252,11 @@ __global__ void __launch_bounds__(288, 1) stream_kernel(const __grid_constant__ 
             }
             // sources of this row: lane j handles slot j (n_slots <= 17 <= 32)
             const void *src = nullptr;
-            if (lane < n_main) {
-                if (kMode == kFold) {
-                    src = p.partials[lane] + (p.in_row0 + row) * p.H;
-                } else {
-                    const int32_t e = __ldg(p.idx + row * p.topk + lane);
-                    if (e >= 0 && static_cast<int64_t>(e) < p.n_expert_rows)
-                        src = p.expert_out + static_cast<int64_t>(e) * p.H;
-                }
-            } else if (lane == n_main && has_res) {
-                src = p.residual_in + row * p.H;
+            if (kMode == kMoe && lane < n_main) {
+                if (e_next >= 0 && static_cast<int64_t>(e_next) < n_experts)
+                    src = experts + static_cast<int64_t>(e_next) * H;
+            } else if (lane_base != nullptr) {
+                src = lane_base + (lane_row0 + row) * H;
             }
             const unsigned valid = __ballot_sync(0xFFFFFFFFu, src != nullptr);
             const uint32_t full = full0 + 8 * s;
@@ -230,12 +268,13 @@ __global__ void __launch_bounds__(288, 1) stream_kernel(const __grid_constant__ 
                 if (lane == 0 && sj != nullptr)
                     bulk_g2s(stage0 + s * stage_bytes + j * slot_bytes, sj, slot_bytes, full);
             }
+            row = next_row(p, row + gridDim.x);
+            if (kMode == kMoe && lane < n_main && row < rows)
+                e_next = __ldg(idx + row * topk + lane);
         }
-        if (!ok) {
-            if (lane == 0) {
-                atomicOr(&g_device_error, kDeviceErrTimeout);
-                abort_flag = 1;
-            }
+        if (!ok && lane == 0) {
+            atomicOr(&g_device_error, kDeviceErrTimeout);
+            abort_flag = 1;
         }
         // Drain: the copies of the last stages issued must land before the CTA ends.
         if (lane == 0) {
@@ -248,32 +287,41 @@ __global__ void __launch_bounds__(288, 1) stream_kernel(const __grid_constant__ 
     }
 
     // -------------------------------- consumers --------------------------------
-    const int ct = threadIdx.x - 32;
+    const int g = (warp - 1) / W;                        // consumer group
+    const int cw = (warp - 1) % W;                       // warp within the group
+    const int ct = cw * 32 + lane;                       // thread within the group
+    const int gthreads = W * 32;
+    const int bar_id = 1 + g;
     const int64_t nvec = p.H >> 3;
+    const bool need_read = kFp8 || p.y_out != nullptr;
     int64_t col[kVpt];
     bool act[kVpt];
     float gm[kVpt][8];
 #pragma unroll
     for (int i = 0; i < kVpt; ++i) {
-        const int64_t v = ct + static_cast<int64_t>(i) * ncthreads;
+        const int64_t v = ct + static_cast<int64_t>(i) * gthreads;
         act[i] = v < nvec;
         col[i] = v * 8;
-        if (act[i] && (kFp8 || p.y_out != nullptr))
+    }
+    pdl_wait();
+#pragma unroll
+    for (int i = 0; i < kVpt; ++i) {
+        if (act[i] && need_read)
             ld_gamma8(p.gamma + col[i], gm[i]);
         else
 #pragma unroll
             for (int e = 0; e < 8; ++e)
                 gm[i][e] = 0.0f;
     }
-    const bool need_read = kFp8 || p.y_out != nullptr;
-    const int cw = warp - 1;
 
-    int used = 0;
+    int par = 0;
+    int i = 0;
     for (int64_t row = next_row(p, blockIdx.x); row < p.rows;
-         row = next_row(p, row + gridDim.x), ++used) {
-        const int s = used % ns;
-        const uint32_t k = static_cast<uint32_t>(used / ns);
-        const int par = used & 1;
+         row = next_row(p, row + gridDim.x), ++i) {
+        if (i % G != g)
+            continue;
+        const int s = i % ns;
+        const uint32_t k = static_cast<uint32_t>(i / ns);
 
         // MoE: routing weights and index validity of this row (broadcast loads,
         // issued before the wait so that their latency hides behind it)
@@ -300,133 +348,138 @@ __global__ void __launch_bounds__(288, 1) stream_kernel(const __grid_constant__ 
             }
         }
 
+        // A thread whose wait fails reads nothing from the stage and writes nothing;
+        // the group learns of it at its row barrier and leaves together.
         const bool ok = mbar_wait_bounded(full0 + 8 * s, k & 1u, &abort_flag);
+        float acc[kVpt][8];
+#pragma unroll
+        for (int v = 0; v < kVpt; ++v)
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                acc[v][e] = 0.0f;
+        if (ok) {
+            const uint8_t *stage = smem + static_cast<size_t>(s) * stage_bytes;
+#pragma unroll
+            for (int j = 0; j < LB_MAX_K; ++j) {
+                if (j >= n_main)
+                    break;
+                if (kMode == kMoe && !okj[j])
+                    continue;
+                const uint8_t *slot = stage + static_cast<size_t>(j) * slot_bytes;
+#pragma unroll
+                for (int v = 0; v < kVpt; ++v)
+                    if (act[v]) {
+                        float f[8];
+                        unpack8(*reinterpret_cast<const uint4 *>(slot + col[v] * 2), f);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            acc[v][e] = (kMode == kMoe)
+                                            ? __fadd_rn(acc[v][e], __fmul_rn(wj[j], f[e]))
+                                            : __fadd_rn(acc[v][e], f[e]);
+                    }
+            }
+            if (has_res) {
+                const uint8_t *slot = stage + static_cast<size_t>(n_main) * slot_bytes;
+#pragma unroll
+                for (int v = 0; v < kVpt; ++v)
+                    if (act[v]) {
+                        float f[8];
+                        unpack8(*reinterpret_cast<const uint4 *>(slot + col[v] * 2), f);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            acc[v][e] = __fadd_rn(acc[v][e], f[e]);
+                    }
+            }
+        }
+        // the stage's data is in registers: hand it back to the producer
         __syncwarp();
-        if (consumer_sync_or(!ok, ncthreads)) {
+        if (ok && lane == 0)
+            mbar_arrive(empty0 + 8 * s);
+        if (ok && p.residual_out != nullptr) {
+#pragma unroll
+            for (int v = 0; v < kVpt; ++v)
+                if (act[v])
+                    *reinterpret_cast<uint4 *>(p.residual_out + row * p.H + col[v]) =
+                        pack8(acc[v]);
+        }
+        if (!need_read) {
+            if (!ok) {
+                atomicOr(&g_device_error, kDeviceErrTimeout);
+                abort_flag = 1;
+                return;
+            }
+            continue;
+        }
+
+        // One barrier per row: sum(o^2) and, for FP8, max|o * gamma| (amax of the read
+        // is r * max|o * gamma| since r > 0), plus the group's verdict on the waits.
+        float ss = 0.0f, mg = 0.0f;
+#pragma unroll
+        for (int v = 0; v < kVpt; ++v)
+            if (act[v])
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    ss = __fmaf_rn(acc[v][e], acc[v][e], ss);
+                    if (kFp8)
+                        mg = fmaxf(mg, fabsf(__fmul_rn(acc[v][e], gm[v][e])));
+                }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            ss += __shfl_xor_sync(0xFFFFFFFFu, ss, off);
+            if (kFp8)
+                mg = fmaxf(mg, __shfl_xor_sync(0xFFFFFFFFu, mg, off));
+        }
+        if (lane == 0)
+            red[g][par][cw] = make_float2(ss, mg);
+        if (group_sync_or(!ok, bar_id, gthreads)) {
             if (ct == 0) {
                 atomicOr(&g_device_error, kDeviceErrTimeout);
                 abort_flag = 1;
             }
             return;
         }
-
-        const uint8_t *stage = smem + static_cast<size_t>(s) * stage_bytes;
-        float acc[kVpt][8];
-#pragma unroll
-        for (int i = 0; i < kVpt; ++i)
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                acc[i][e] = 0.0f;
-#pragma unroll
-        for (int j = 0; j < LB_MAX_K; ++j) {
-            if (j >= n_main)
-                break;
-            if (kMode == kMoe && !okj[j])
-                continue;
-            const uint8_t *slot = stage + static_cast<size_t>(j) * slot_bytes;
-#pragma unroll
-            for (int i = 0; i < kVpt; ++i)
-                if (act[i]) {
-                    float f[8];
-                    unpack8(*reinterpret_cast<const uint4 *>(slot + col[i] * 2), f);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        acc[i][e] = (kMode == kMoe)
-                                        ? __fadd_rn(acc[i][e], __fmul_rn(wj[j], f[e]))
-                                        : __fadd_rn(acc[i][e], f[e]);
-                }
+        float2 t = red[g][par][0];
+        ss = t.x;
+        mg = t.y;
+        for (int w = 1; w < W; ++w) {
+            t = red[g][par][w];
+            ss += t.x;
+            mg = fmaxf(mg, t.y);
         }
-        if (has_res) {
-            const uint8_t *slot = stage + static_cast<size_t>(n_main) * slot_bytes;
-#pragma unroll
-            for (int i = 0; i < kVpt; ++i)
-                if (act[i]) {
-                    float f[8];
-                    unpack8(*reinterpret_cast<const uint4 *>(slot + col[i] * 2), f);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        acc[i][e] = __fadd_rn(acc[i][e], f[e]);
-                }
-        }
-        // the stage's data is in registers: hand it back to the producer
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(empty0 + 8 * s);
-
-        if (p.residual_out != nullptr) {
-#pragma unroll
-            for (int i = 0; i < kVpt; ++i)
-                if (act[i])
-                    *reinterpret_cast<uint4 *>(p.residual_out + row * p.H + col[i]) =
-                        pack8(acc[i]);
-        }
-        if (!need_read)
-            continue;
-
-        // r = 1/sqrt(mean(o^2) + eps)
-        float ss = 0.0f;
-#pragma unroll
-        for (int i = 0; i < kVpt; ++i)
-            if (act[i])
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    ss = __fmaf_rn(acc[i][e], acc[i][e], ss);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-            ss += __shfl_xor_sync(0xFFFFFFFFu, ss, off);
-        if (lane == 0)
-            red_ss[par][cw] = ss;
-        consumer_sync(ncthreads);
-        ss = red_ss[par][0];
-        for (int w = 1; w < ncw; ++w)
-            ss += red_ss[par][w];
+        par ^= 1;
         const float r = rsqrtf(__fmaf_rn(ss, p.inv_H, p.eps));
 
 #pragma unroll
-        for (int i = 0; i < kVpt; ++i)
+        for (int v = 0; v < kVpt; ++v)
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-                acc[i][e] = __fmul_rn(__fmul_rn(acc[i][e], r), gm[i][e]);
+                acc[v][e] = __fmul_rn(__fmul_rn(acc[v][e], r), gm[v][e]);
 
         if (p.y_out != nullptr) {
 #pragma unroll
-            for (int i = 0; i < kVpt; ++i)
-                if (act[i])
-                    *reinterpret_cast<uint4 *>(p.y_out + row * p.H + col[i]) = pack8(acc[i]);
+            for (int v = 0; v < kVpt; ++v)
+                if (act[v])
+                    *reinterpret_cast<uint4 *>(p.y_out + row * p.H + col[v]) = pack8(acc[v]);
         }
         if (!kFp8)
             continue;
 
-        float mx = 0.0f;
-#pragma unroll
-        for (int i = 0; i < kVpt; ++i)
-            if (act[i])
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    mx = fmaxf(mx, fabsf(acc[i][e]));
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
-        if (lane == 0)
-            red_mx[par][cw] = mx;
-        consumer_sync(ncthreads);
-        mx = red_mx[par][0];
-        for (int w = 1; w < ncw; ++w)
-            mx = fmaxf(mx, red_mx[par][w]);
-        const bool nonzero = mx > 0.0f;
-        const float inv = nonzero ? __fdividef(448.0f, mx) : 0.0f;
+        // FP8 read: scale = amax / 448, q = E4M3(yf * 448 / amax)
+        const float amax = __fmul_rn(r, mg);
+        const bool nonzero = amax > 0.0f;
+        const float inv = nonzero ? __fdividef(448.0f, amax) : 0.0f;
         if (ct == 0)
-            p.scale_out[row] = mx / 448.0f;
+            p.scale_out[row] = amax / 448.0f;
 #pragma unroll
-        for (int i = 0; i < kVpt; ++i)
-            if (act[i]) {
-                float v[8];
+        for (int v = 0; v < kVpt; ++v)
+            if (act[v]) {
+                float q[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
-                    v[e] = nonzero ? __fmul_rn(acc[i][e], inv) : 0.0f;
-                const uint32_t lo = cvt_e4m3x2(v[0], v[1]) | (cvt_e4m3x2(v[2], v[3]) << 16);
-                const uint32_t hi = cvt_e4m3x2(v[4], v[5]) | (cvt_e4m3x2(v[6], v[7]) << 16);
-                *reinterpret_cast<uint2 *>(p.q_out + row * p.H + col[i]) = make_uint2(lo, hi);
+                    q[e] = nonzero ? __fmul_rn(acc[v][e], inv) : 0.0f;
+                const uint32_t lo = cvt_e4m3x2(q[0], q[1]) | (cvt_e4m3x2(q[2], q[3]) << 16);
+                const uint32_t hi = cvt_e4m3x2(q[4], q[5]) | (cvt_e4m3x2(q[6], q[7]) << 16);
+                *reinterpret_cast<uint2 *>(p.q_out + row * p.H + col[v]) = make_uint2(lo, hi);
             }
     }
 }
@@ -444,10 +497,16 @@ cudaError_t launch_stream_variant(const Params &p, const StreamShape &s, cudaStr
         return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(s.grid), 1, 1);
-    cfg.blockDim = dim3(static_cast<unsigned>(32 * (1 + s.consumer_warps)), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(32 * (1 + s.groups * s.consumer_warps)), 1, 1);
+    if (cfg.blockDim.x > static_cast<unsigned>(StreamThreads<kVpt>::value))
+        return cudaErrorInvalidConfiguration;
     cfg.dynamicSmemBytes = static_cast<size_t>(s.smem_bytes);
     cfg.stream = stream;
-    cfg.numAttrs = 0;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 

@@ -29,6 +29,7 @@ LB_MAX_H = 131072
 LB_KERNEL_ROW = 0
 LB_KERNEL_STREAM = 1
 LB_DEVICE_ERR_TIMEOUT = 1
+LB_DEVICE_ERR_LAUNCH = 2
 
 EXPORTED = ("lb_status_string", "lb_last_cuda_error", "lb_version", "lb_launch_plan",
             "lb_device_error", "lb_fold_norm", "lb_fold_norm_fp8",

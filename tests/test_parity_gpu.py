@@ -311,6 +311,52 @@ def test_moe_bad_index_on_the_stream_kernel(lb):
     check_fold(got, want, "moe bad index, stream kernel")
 
 
+def test_dependent_chain_of_boundaries(lb):
+    """Layers back to back on one stream with no host synchronisation: each boundary
+    reads the residual the previous one wrote, and a torch kernel writes the next
+    partials just before each call (the kernels are programmatic dependents of the
+    previous launch, so this checks that every read waits for its producer)."""
+    rows = (2048, 64, 700, 1024, 2048)           # stream, row, stream, MoE, stream kernels
+    H = 1024
+    rng = np.random.default_rng(81)
+    gamma = (1 + 0.1 * rng.standard_normal(H)).astype(np.float32)
+    res_host = wl.to_bf16_bits(rng.standard_normal((max(rows), H)).astype(np.float32))
+    G = torch.from_numpy(gamma).cuda()
+    R = dev_bits(res_host)
+    want_res = res_host.copy()
+    ys = []
+    for li, T in enumerate(rows):
+        seeds = [1000 * li + k for k in range(3)]
+        P_host = [wl.to_bf16_bits(np.random.default_rng(sd).standard_normal((T, H))
+                                  .astype(np.float32)) for sd in seeds]
+        P = [torch.empty((T, H), dtype=torch.bfloat16, device="cuda") for _ in seeds]
+        for d, h in zip(P, P_host):               # written by torch right before the call
+            d.view(torch.int16).copy_(torch.from_numpy(h.view(np.int16)).cuda() * 1)
+        Rn = torch.empty_like(R)
+        Y = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+        if li == 3:                                # a MoE finalize layer
+            idx = torch.arange(T * 3, dtype=torch.int32, device="cuda").view(T, 3)
+            E = torch.cat(P, dim=1).view(T * 3, H)
+            wts = torch.full((T, 3), 1.0, dtype=torch.float32, device="cuda")
+            lb.lb_moe_finalize_fold_norm(E, T * 3, idx, wts, 3, R[:T], Rn[:T], G, Y, None,
+                                         None, T, H, 1e-6)
+            Eh = np.stack(P_host, axis=1).reshape(T * 3, H)
+            o = oracle.moe_finalize_fold_norm(Eh, np.arange(T * 3, dtype=np.int32)
+                                              .reshape(T, 3), np.ones((T, 3), np.float32),
+                                              want_res[:T], gamma, 1e-6)
+        else:
+            lb.lb_fold_norm(P, R[:T], Rn[:T], G, Y, T, H, 1e-6)
+            o = oracle.fold_norm(P_host, want_res[:T], gamma, 1e-6)
+        Rn[T:] = R[T:]
+        R = Rn
+        want_res[:T] = o["residual_out"]
+        ys.append((Y, o["y"]))
+    torch.cuda.synchronize()
+    assert_bits_equal(host_bits(R), want_res, "chained residual'")
+    for li, (Y, want_y) in enumerate(ys):
+        assert_bf16_close(host_bits(Y), want_y, f"chained layer {li} y")
+
+
 def test_specified_workloads_take_the_intended_kernels(lb):
     assert plan(lb, 2048, 4096, 5).kernel == lb.LB_KERNEL_STREAM     # prefill
     assert plan(lb, 1024, 4096, 9).kernel == lb.LB_KERNEL_STREAM     # MoE finalize
