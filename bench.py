@@ -216,6 +216,12 @@ def plan_of(lb, rows, H, n_inputs, props):
     return lb.lb_launch_plan(rows, H, n_inputs, props.multi_processor_count, smem).as_dict()
 
 
+def kernel_name(plan, mode, fp8):
+    kind = "stream_kernel" if plan["kernel"] == 1 else "boundary_kernel"
+    return (f"{kind}<{mode}, {'fp8' if fp8 else 'bf16'}, "
+            f"{plan['vectors_per_thread']} vectors/thread>")
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     files = sorted(glob.glob(os.path.join(ROOT, "layer_boundary_fusion_gb300", "csrc", "*")))
@@ -478,7 +484,7 @@ def run_native(args, dist):
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": ncu_traffic(HEADLINE), "peak_source": peak_src,
                      "algorithmic_bytes_per_launch": nbytes,
-                     "kernel": "boundary_kernel<fold, fp8, 1 vector/thread>"},
+                     "kernel": kernel_name(plan_of(lb, w.T, w.H, w.K + 1, props), "fold", True)},
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps},

@@ -87,6 +87,7 @@ typedef struct {
     int ctas_per_row;       /* row kernel: CTAs (cluster size) per row; else 1 */
     int stages;             /* stream kernel: shared-memory stages; else 0 */
     int smem_bytes;         /* stream kernel: dynamic shared memory per CTA; else 0 */
+    int groups;             /* stream kernel: consumer groups (rows reduced at once) */
 } lb_plan;
 
 /*

@@ -253,7 +253,8 @@ bool choose_stream_shape(int64_t rows, int64_t H, int n_inputs, int num_sms,
         return false;
     const int64_t nvec = H / 8;
     const int64_t maxw = LB_STREAM_CONSUMER_WARPS;
-    const int ncw = static_cast<int>(nvec >= 32 * maxw ? maxw : (nvec + 31) / 32);
+    int ncw = static_cast<int>(nvec >= 32 * maxw ? maxw : (nvec + 31) / 32);
+    ncw += ncw & 1;                            // an even number of warps per group
     int64_t vpt = (nvec + ncw * 32 - 1) / (ncw * 32);
     if (vpt > 4)
         return false;
@@ -272,7 +273,7 @@ bool choose_stream_shape(int64_t rows, int64_t H, int n_inputs, int num_sms,
     // multiple of the group count, so that every stage belongs to one group and its
     // uses are consumed in order: a parity wait on an mbarrier tells only two
     // consecutive phases apart.
-    int64_t groups = vpt >= 4 ? 1 : LB_STREAM_GROUPS;
+    int64_t groups = vpt >= 4 ? LB_STREAM_GROUPS_WIDE : LB_STREAM_GROUPS;
     if (groups > ns)
         groups = ns;
     ns -= ns % groups;
@@ -353,6 +354,7 @@ lb_status lb_launch_plan(int64_t rows, int64_t H, int n_inputs, int num_sms,
         plan->ctas_per_row = 1;
         plan->stages = ss.stages;
         plan->smem_bytes = ss.smem_bytes;
+        plan->groups = ss.groups;
         return LB_OK;
     }
     lb::Shape s;

@@ -18,7 +18,11 @@
 #define LB_STREAM_CONSUMER_WARPS 8
 #endif
 #ifndef LB_STREAM_GROUPS
-#define LB_STREAM_GROUPS 2
+#define LB_STREAM_GROUPS 3
+#endif
+// consumer groups when each thread owns four vectors (long rows: more registers)
+#ifndef LB_STREAM_GROUPS_WIDE
+#define LB_STREAM_GROUPS_WIDE 1
 #endif
 #ifndef LB_STREAM_MAX_STAGES
 #define LB_STREAM_MAX_STAGES 8

@@ -107,6 +107,47 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     return false;
 }
 
+// 16 bytes from this CTA's shared memory (32-bit shared-window address).
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+// 8 bf16 (element 0 in the low half of .x) -> 4 binary32 pairs; widening is exact.
+__device__ __forceinline__ void unpack8x2(const uint4 &w, float2 f[4]) {
+    f[0] = make_float2(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u));
+    f[1] = make_float2(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
+    f[2] = make_float2(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xFFFF0000u));
+    f[3] = make_float2(__uint_as_float(w.w << 16), __uint_as_float(w.w & 0xFFFF0000u));
+}
+
+__device__ __forceinline__ uint4 pack8x2(const float2 f[4]) {
+    return make_uint4(pack_bf16x2(f[0].x, f[0].y), pack_bf16x2(f[1].x, f[1].y),
+                      pack_bf16x2(f[2].x, f[2].y), pack_bf16x2(f[3].x, f[3].y));
+}
+
+// acc + w * f with the product rounded to binary32 before the add, per lane (the
+// MoE finalize's definition).  ptxas turns a packed f32x2 multiply feeding a packed
+// add into a packed fused multiply-add even when both carry .rn, so the two
+// products are formed with scalar mul.rn.f32 (never fused) and only the add is
+// packed; the parity tests check residual' bit for bit against the definition.
+__device__ __forceinline__ float2 add_mul2_rn(float2 acc, float w, float2 f) {
+    float2 r;
+    asm("{\n\t.reg .b64 a, t;\n\t.reg .f32 px, py;\n\t"
+        "mul.rn.f32 px, %4, %5;\n\t"
+        "mul.rn.f32 py, %4, %6;\n\t"
+        "mov.b64 a, {%2, %3};\n\t"
+        "mov.b64 t, {px, py};\n\t"
+        "add.rn.f32x2 t, a, t;\n\t"
+        "mov.b64 {%0, %1}, t;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(acc.x), "f"(acc.y), "f"(w), "f"(f.x), "f"(f.y));
+    return r;
+}
+
 // One bulk copy global -> this CTA's shared memory, completing on `bar`.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
                                          uint32_t bar) {
@@ -137,6 +178,15 @@ __device__ __forceinline__ int64_t next_row(const Params &p, int64_t row) {
     return row;
 }
 
+// The valid row `n` places after `row` in this CTA's sequence.
+__device__ __forceinline__ int64_t advance(const Params &p, int64_t row, int n) {
+    if (p.num_sets == 0)
+        return row + static_cast<int64_t>(n) * gridDim.x;
+    for (int t = 0; t < n && row < p.rows; ++t)
+        row = next_row(p, row + gridDim.x);
+    return row;
+}
+
 // ------------------------------------------------------------------------------------
 // The kernel
 // ------------------------------------------------------------------------------------
@@ -145,9 +195,18 @@ __device__ __forceinline__ int64_t next_row(const Params &p, int64_t row) {
 // groups.  Four-vector threads need more registers and run one group.
 template <int kVpt>
 struct StreamThreads {
-    static constexpr int groups = (kVpt >= 4) ? 1 : LB_STREAM_GROUPS;
+    static constexpr int groups = (kVpt >= 4) ? LB_STREAM_GROUPS_WIDE : LB_STREAM_GROUPS;
     static constexpr int value = 32 * (1 + groups * LB_STREAM_CONSUMER_WARPS);
 };
+constexpr int kGroupsMax =
+    LB_STREAM_GROUPS > LB_STREAM_GROUPS_WIDE ? LB_STREAM_GROUPS : LB_STREAM_GROUPS_WIDE;
+
+// Maximum over the warp of a non-negative float (one redux instruction).
+__device__ __forceinline__ float warp_max(float v) {
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
 
 // Group-local barrier that also ORs a predicate over the group (barrier id 1 + g).
 __device__ __forceinline__ bool group_sync_or(bool pred, int id, int nthreads) {
@@ -176,7 +235,7 @@ template <int kMode, bool kFp8, int kVpt>
 __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
     stream_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ float2 red[LB_STREAM_GROUPS][2][LB_STREAM_CONSUMER_WARPS];
+    __shared__ __align__(16) float2 red[kGroupsMax][2][LB_STREAM_CONSUMER_WARPS];
     __shared__ int abort_flag;
 
     const int warp = threadIdx.x >> 5;
@@ -295,33 +354,48 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
     const int64_t nvec = p.H >> 3;
     const bool need_read = kFp8 || p.y_out != nullptr;
     int64_t col[kVpt];
+    uint32_t soff[kVpt];                                 // byte offset within a slot
     bool act[kVpt];
-    float gm[kVpt][8];
+    float2 gm[kVpt][4];
 #pragma unroll
     for (int i = 0; i < kVpt; ++i) {
         const int64_t v = ct + static_cast<int64_t>(i) * gthreads;
         act[i] = v < nvec;
         col[i] = v * 8;
+        soff[i] = static_cast<uint32_t>(v * 16);
     }
     pdl_wait();
 #pragma unroll
     for (int i = 0; i < kVpt; ++i) {
-        if (act[i] && need_read)
-            ld_gamma8(p.gamma + col[i], gm[i]);
-        else
+        if (act[i] && need_read) {
+            const float4 a = __ldg(reinterpret_cast<const float4 *>(p.gamma + col[i]));
+            const float4 b = __ldg(reinterpret_cast<const float4 *>(p.gamma + col[i]) + 1);
+            gm[i][0] = make_float2(a.x, a.y);
+            gm[i][1] = make_float2(a.z, a.w);
+            gm[i][2] = make_float2(b.x, b.y);
+            gm[i][3] = make_float2(b.z, b.w);
+        } else {
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-                gm[i][e] = 0.0f;
+            for (int e = 0; e < 4; ++e)
+                gm[i][e] = make_float2(0.0f, 0.0f);
+        }
     }
 
+    // This group's rows are the CTA's valid rows g, g + G, g + 2G, ...; with the
+    // stage count a multiple of G, the group's stage advances by G per row and the
+    // phase parity flips each time it wraps.
+    int s = g;
+    uint32_t phase = 0;
     int par = 0;
-    int i = 0;
-    for (int64_t row = next_row(p, blockIdx.x); row < p.rows;
-         row = next_row(p, row + gridDim.x), ++i) {
-        if (i % G != g)
-            continue;
-        const int s = i % ns;
-        const uint32_t k = static_cast<uint32_t>(i / ns);
+    int64_t row = next_row(p, blockIdx.x);
+    for (int t = 0; t < g && row < p.rows; ++t)
+        row = next_row(p, row + gridDim.x);
+    for (; row < p.rows; s += G) {
+        if (s >= ns) {
+            s -= ns;
+            phase ^= 1u;
+        }
+        const uint32_t k = phase;
 
         // MoE: routing weights and index validity of this row (broadcast loads,
         // issued before the wait so that their latency hides behind it)
@@ -351,43 +425,45 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
         // A thread whose wait fails reads nothing from the stage and writes nothing;
         // the group learns of it at its row barrier and leaves together.
         const bool ok = mbar_wait_bounded(full0 + 8 * s, k & 1u, &abort_flag);
-        float acc[kVpt][8];
+        // o in binary32 pairs: acc[v][i] holds elements 2i, 2i+1 of vector v.  Packed
+        // f32x2 adds and multiplies round each lane exactly like the scalar ones, so
+        // the order of the definition -- and residual' bit for bit -- is kept.
+        float2 acc[kVpt][4];
 #pragma unroll
         for (int v = 0; v < kVpt; ++v)
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-                acc[v][e] = 0.0f;
+            for (int e = 0; e < 4; ++e)
+                acc[v][e] = make_float2(0.0f, 0.0f);
         if (ok) {
-            const uint8_t *stage = smem + static_cast<size_t>(s) * stage_bytes;
+            const uint32_t stage = stage0 + static_cast<uint32_t>(s) * stage_bytes;
 #pragma unroll
             for (int j = 0; j < LB_MAX_K; ++j) {
                 if (j >= n_main)
                     break;
                 if (kMode == kMoe && !okj[j])
                     continue;
-                const uint8_t *slot = stage + static_cast<size_t>(j) * slot_bytes;
+                const uint32_t slot = stage + static_cast<uint32_t>(j) * slot_bytes;
 #pragma unroll
                 for (int v = 0; v < kVpt; ++v)
                     if (act[v]) {
-                        float f[8];
-                        unpack8(*reinterpret_cast<const uint4 *>(slot + col[v] * 2), f);
+                        float2 f[4];
+                        unpack8x2(lds128(slot + soff[v]), f);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            acc[v][e] = (kMode == kMoe)
-                                            ? __fadd_rn(acc[v][e], __fmul_rn(wj[j], f[e]))
-                                            : __fadd_rn(acc[v][e], f[e]);
+                        for (int e = 0; e < 4; ++e)
+                            acc[v][e] = (kMode == kMoe) ? add_mul2_rn(acc[v][e], wj[j], f[e])
+                                                        : __fadd2_rn(acc[v][e], f[e]);
                     }
             }
             if (has_res) {
-                const uint8_t *slot = stage + static_cast<size_t>(n_main) * slot_bytes;
+                const uint32_t slot = stage + static_cast<uint32_t>(n_main) * slot_bytes;
 #pragma unroll
                 for (int v = 0; v < kVpt; ++v)
                     if (act[v]) {
-                        float f[8];
-                        unpack8(*reinterpret_cast<const uint4 *>(slot + col[v] * 2), f);
+                        float2 f[4];
+                        unpack8x2(lds128(slot + soff[v]), f);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            acc[v][e] = __fadd_rn(acc[v][e], f[e]);
+                        for (int e = 0; e < 4; ++e)
+                            acc[v][e] = __fadd2_rn(acc[v][e], f[e]);
                     }
             }
         }
@@ -395,12 +471,13 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
         __syncwarp();
         if (ok && lane == 0)
             mbar_arrive(empty0 + 8 * s);
+        const int64_t roff = row * p.H;
         if (ok && p.residual_out != nullptr) {
 #pragma unroll
             for (int v = 0; v < kVpt; ++v)
                 if (act[v])
-                    *reinterpret_cast<uint4 *>(p.residual_out + row * p.H + col[v]) =
-                        pack8(acc[v]);
+                    *reinterpret_cast<uint4 *>(p.residual_out + roff + col[v]) =
+                        pack8x2(acc[v]);
         }
         if (!need_read) {
             if (!ok) {
@@ -408,27 +485,31 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
                 abort_flag = 1;
                 return;
             }
+            row = advance(p, row, G);
             continue;
         }
 
         // One barrier per row: sum(o^2) and, for FP8, max|o * gamma| (amax of the read
         // is r * max|o * gamma| since r > 0), plus the group's verdict on the waits.
-        float ss = 0.0f, mg = 0.0f;
+        float2 ss2 = make_float2(0.0f, 0.0f);
+        float mg = 0.0f;
 #pragma unroll
         for (int v = 0; v < kVpt; ++v)
             if (act[v])
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    ss = __fmaf_rn(acc[v][e], acc[v][e], ss);
-                    if (kFp8)
-                        mg = fmaxf(mg, fabsf(__fmul_rn(acc[v][e], gm[v][e])));
+                for (int e = 0; e < 4; ++e) {
+                    ss2 = __ffma2_rn(acc[v][e], acc[v][e], ss2);
+                    if (kFp8) {
+                        const float2 t = __fmul2_rn(acc[v][e], gm[v][e]);
+                        mg = fmaxf(mg, fmaxf(fabsf(t.x), fabsf(t.y)));
+                    }
                 }
+        float ss = ss2.x + ss2.y;
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
+        for (int off = 16; off > 0; off >>= 1)
             ss += __shfl_xor_sync(0xFFFFFFFFu, ss, off);
-            if (kFp8)
-                mg = fmaxf(mg, __shfl_xor_sync(0xFFFFFFFFu, mg, off));
-        }
+        if (kFp8)
+            mg = warp_max(mg);
         if (lane == 0)
             red[g][par][cw] = make_float2(ss, mg);
         if (group_sync_or(!ok, bar_id, gthreads)) {
@@ -438,49 +519,66 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
             }
             return;
         }
-        float2 t = red[g][par][0];
-        ss = t.x;
-        mg = t.y;
-        for (int w = 1; w < W; ++w) {
-            t = red[g][par][w];
+        // the group's W (even) slots, two per 16-byte read, summed in warp order
+        const float4 *slots = reinterpret_cast<const float4 *>(&red[g][par][0]);
+        ss = 0.0f;
+        mg = 0.0f;
+        for (int w = 0; w < (W >> 1); ++w) {
+            const float4 t = slots[w];
             ss += t.x;
-            mg = fmaxf(mg, t.y);
+            ss += t.z;
+            mg = fmaxf(mg, fmaxf(t.y, t.w));
         }
         par ^= 1;
         const float r = rsqrtf(__fmaf_rn(ss, p.inv_H, p.eps));
+        const float2 r2 = make_float2(r, r);
 
+        // yf = (o * r) * gamma
 #pragma unroll
         for (int v = 0; v < kVpt; ++v)
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-                acc[v][e] = __fmul_rn(__fmul_rn(acc[v][e], r), gm[v][e]);
+            for (int e = 0; e < 4; ++e)
+                acc[v][e] = __fmul2_rn(__fmul2_rn(acc[v][e], r2), gm[v][e]);
 
         if (p.y_out != nullptr) {
 #pragma unroll
             for (int v = 0; v < kVpt; ++v)
                 if (act[v])
-                    *reinterpret_cast<uint4 *>(p.y_out + row * p.H + col[v]) = pack8(acc[v]);
+                    *reinterpret_cast<uint4 *>(p.y_out + roff + col[v]) = pack8x2(acc[v]);
         }
-        if (!kFp8)
+        if (!kFp8) {
+            row = advance(p, row, G);
             continue;
+        }
 
-        // FP8 read: scale = amax / 448, q = E4M3(yf * 448 / amax)
+        // FP8 read: scale = amax / 448, q = E4M3(yf * 448 / amax); an all-zero row
+        // (amax = 0) gets scale 0 and codes 0x00.
         const float amax = __fmul_rn(r, mg);
-        const bool nonzero = amax > 0.0f;
-        const float inv = nonzero ? __fdividef(448.0f, amax) : 0.0f;
         if (ct == 0)
             p.scale_out[row] = amax / 448.0f;
+        if (amax > 0.0f) {
+            const float inv = __fdividef(448.0f, amax);
+            const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
-        for (int v = 0; v < kVpt; ++v)
-            if (act[v]) {
-                float q[8];
+            for (int v = 0; v < kVpt; ++v)
+                if (act[v]) {
+                    float2 q[4];
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    q[e] = nonzero ? __fmul_rn(acc[v][e], inv) : 0.0f;
-                const uint32_t lo = cvt_e4m3x2(q[0], q[1]) | (cvt_e4m3x2(q[2], q[3]) << 16);
-                const uint32_t hi = cvt_e4m3x2(q[4], q[5]) | (cvt_e4m3x2(q[6], q[7]) << 16);
-                *reinterpret_cast<uint2 *>(p.q_out + row * p.H + col[v]) = make_uint2(lo, hi);
-            }
+                    for (int e = 0; e < 4; ++e)
+                        q[e] = __fmul2_rn(acc[v][e], inv2);
+                    const uint32_t lo = cvt_e4m3x2(q[0].x, q[0].y) |
+                                        (cvt_e4m3x2(q[1].x, q[1].y) << 16);
+                    const uint32_t hi = cvt_e4m3x2(q[2].x, q[2].y) |
+                                        (cvt_e4m3x2(q[3].x, q[3].y) << 16);
+                    *reinterpret_cast<uint2 *>(p.q_out + roff + col[v]) = make_uint2(lo, hi);
+                }
+        } else {
+#pragma unroll
+            for (int v = 0; v < kVpt; ++v)
+                if (act[v])
+                    *reinterpret_cast<uint2 *>(p.q_out + roff + col[v]) = make_uint2(0u, 0u);
+        }
+        row = advance(p, row, G);
     }
 }
 

@@ -67,9 +67,9 @@ SMEM = 232448          # opt-in shared memory per CTA on GB300
 
 @pytest.mark.parametrize("rows,H,n_in,plan", [
     # (kernel, grid, threads, vectors/thread, ctas/row, stages, smem)
-    (2048, 4096, 5, (1, 152, 544, 2, 1, 4, 163904)),    # prefill K=4 + residual: stream
-    (1024, 4096, 9, (1, 152, 544, 2, 1, 2, 147488)),    # MoE top-8 + residual: stream
-    (254, 4096, 9, (1, 152, 544, 2, 1, 2, 147488)),     # one ragged slice: stream
+    (2048, 4096, 5, (1, 152, 800, 2, 1, 3, 122928)),    # prefill K=4 + residual: stream
+    (1024, 4096, 9, (1, 152, 800, 2, 1, 3, 221232)),    # MoE top-8 + residual: stream
+    (254, 4096, 9, (1, 152, 800, 2, 1, 3, 221232)),     # one ragged slice: stream
     (64, 4096, 9, (0, 512, 64, 1, 8, 0, 0)),            # decode: 8-CTA clusters per row
     (1, 4096, 2, (0, 8, 64, 1, 8, 0, 0)),
     (16, 512, 3, (0, 16, 64, 1, 1, 0, 0)),              # tiny: one CTA per row
@@ -77,8 +77,8 @@ SMEM = 232448          # opt-in shared memory per CTA on GB300
     (4096, 8192, 9, (0, 4096, 512, 2, 1, 0, 0)),        # no double-buffered stage fits
     (4096, 16384, 3, (0, 4096, 512, 4, 1, 0, 0)),
     (4096, 32768, 2, (0, 8192, 512, 4, 2, 0, 0)),
-    (4096, 520, 2, (1, 152, 224, 1, 1, 8, 16768)),      # 65 vectors: partly active warp
-    (4096, 8, 2, (1, 152, 96, 1, 1, 8, 384)),
+    (4096, 520, 2, (1, 152, 416, 1, 1, 6, 12576)),      # 65 vectors: partly active warp
+    (4096, 8, 2, (1, 152, 224, 1, 1, 6, 288)),
 ])
 def test_launch_plan(lib, rows, H, n_in, plan):
     p = lib.lb_launch_plan(rows, H, n_in, 152, SMEM)
@@ -100,7 +100,8 @@ def test_launch_plan_covers_every_row_vector(lib):
                     assert p.ctas_per_row * per_cta >= nvec and 1 <= p.ctas_per_row <= 8
                     assert p.grid == rows * p.ctas_per_row
                 else:
-                    groups = 1 if p.vectors_per_thread == 4 else 2
+                    groups = p.groups
+                    assert groups == (1 if p.vectors_per_thread == 4 else min(3, p.stages))
                     consumers = (p.threads - 32) // groups
                     assert consumers % 32 == 0 and 32 <= consumers <= 256
                     assert consumers * p.vectors_per_thread >= nvec
