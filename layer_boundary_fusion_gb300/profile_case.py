@@ -31,13 +31,16 @@ def make_launcher(name, row_scale, dev, stream):
     G = torch.from_numpy(w.gamma).to(dev)
     if name == "moe_finalize":
         T = w.T * row_scale
-        E = _bits(w.expert_out, dev)
-        idx = torch.from_numpy(_rep(w.idx, row_scale)).to(dev)
+        n_rows = w.expert_out.shape[0]
+        E = _bits(_rep(w.expert_out, row_scale), dev)
+        # copy r of the tokens gathers from copy r of the expert rows: no row is read twice
+        idx = np.concatenate([w.idx + r * n_rows for r in range(row_scale)]).astype(np.int32)
+        idx = torch.from_numpy(idx).to(dev)
         wt = torch.from_numpy(_rep(w.w, row_scale)).to(dev)
         R = _bits(_rep(w.residual, row_scale), dev)
         ro, yo = torch.empty_like(R), torch.empty_like(R)
         return T, lambda: lb.lb_moe_finalize_fold_norm(
-            E, w.expert_out.shape[0], idx, wt, w.topk, R, ro, G, yo, None, None, T, w.H, w.eps,
+            E, n_rows * row_scale, idx, wt, w.topk, R, ro, G, yo, None, None, T, w.H, w.eps,
             None, stream=sp)
     if name == "ragged_slice":
         P = [_bits(p, dev) for p in w.partials]
