@@ -264,7 +264,8 @@ bool choose_stream_shape(int64_t rows, int64_t H, int n_inputs, int num_sms,
     int64_t per_cta = LB_SMEM_PER_SM / LB_STREAM_CTAS_PER_SM - 1024;
     if (per_cta > smem_per_block)
         per_cta = smem_per_block;
-    int64_t ns = (per_cta - reserve) / (stage + 16);
+    // per stage: its input rows, two mbarriers and an 80-byte metadata block
+    int64_t ns = (per_cta - reserve) / (stage + 96);
     if (ns > LB_STREAM_MAX_STAGES)
         ns = LB_STREAM_MAX_STAGES;
     if (ns < 2)
@@ -292,7 +293,7 @@ bool choose_stream_shape(int64_t rows, int64_t H, int n_inputs, int num_sms,
     out->consumer_warps = ncw;
     out->vpt = static_cast<int>(vpt);
     out->stages = static_cast<int>(ns);
-    out->smem_bytes = static_cast<int>(ns * stage + 16 * ns);
+    out->smem_bytes = static_cast<int>(ns * (stage + 96));
     return true;
 }
 

@@ -191,6 +191,13 @@ __device__ __forceinline__ int64_t advance(const Params &p, int64_t row, int n) 
 // The kernel
 // ------------------------------------------------------------------------------------
 
+struct StageMeta {
+    float w[LB_MAX_TOPK];
+    uint32_t valid;
+    uint32_t pad[3];
+};
+static_assert(sizeof(StageMeta) == 80, "stage metadata size");
+
 // Threads per CTA the kernel is compiled for: one producer warp plus the consumer
 // groups.  Four-vector threads need more registers and run one group.
 template <int kVpt>
@@ -222,7 +229,8 @@ __device__ __forceinline__ bool group_sync_or(bool pred, int id, int nthreads) {
     return out != 0;
 }
 
-// Shared-memory layout (dynamic): [stages][slot][slot_bytes] then the mbarriers.
+// Shared-memory layout (dynamic): [stages][slot][slot_bytes], the mbarriers (full,
+// empty), then one StageMeta per stage.
 // Slot j < n_main holds partial j (fold) or routed row j (MoE); the residual row, if
 // any, is slot n_main.  The CTA's rows are numbered i = 0, 1, ... in the order the
 // producer streams them; stage i % stages holds row i, and consumer group i % groups
@@ -252,6 +260,9 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
     const uint32_t full0 = smem_addr(bars);
     const uint32_t empty0 = smem_addr(bars + ns);
     const uint32_t stage0 = smem_addr(smem);
+    // MoE: per stage, the row's routing weights and the mask of valid expert indices,
+    // written by the producer before it arms the stage's "full" barrier.
+    StageMeta *meta = reinterpret_cast<StageMeta *>(bars + 2 * ns);
 
     if (G < 1 || ns % G != 0) {                           // launch contract, see above
         if (threadIdx.x == 0)
@@ -297,11 +308,14 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
         // MoE: each lane < topk holds the expert row of its slot, loaded one row ahead
         // so that the index latency hides behind the wait for a free stage.
         int32_t e_next = -1;
-        if (kMode == kMoe && lane < n_main && row < rows)
+        float w_next = 0.0f;
+        if (kMode == kMoe && lane < n_main && row < rows) {
             e_next = __ldg(idx + row * topk + lane);
+            w_next = __ldg(p.w + row * topk + lane);
+        }
+        int s = 0;                       // stage of the next row to issue
+        uint32_t k = 0;                  // use of that stage
         for (; row < rows; ++issued) {
-            const int s = issued % ns;
-            const uint32_t k = static_cast<uint32_t>(issued / ns);
             bool free_ok = true;
             if (k > 0 && lane == 0)
                 free_ok = mbar_wait_bounded(empty0 + 8 * s, (k - 1) & 1u, &abort_flag);
@@ -309,6 +323,7 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
                 ok = false;
                 break;
             }
+            const uint32_t full = full0 + 8 * s;
             // sources of this row: lane j handles slot j (n_slots <= 17 <= 32)
             const void *src = nullptr;
             if (kMode == kMoe && lane < n_main) {
@@ -318,18 +333,35 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
                 src = lane_base + (lane_row0 + row) * H;
             }
             const unsigned valid = __ballot_sync(0xFFFFFFFFu, src != nullptr);
-            const uint32_t full = full0 + 8 * s;
+            if (kMode == kMoe) {
+                if (lane < n_main)
+                    meta[s].w[lane] = w_next;
+                if (lane == 0) {
+                    const unsigned main_mask = (n_main >= 32) ? 0xFFFFFFFFu : ((1u << n_main) - 1u);
+                    meta[s].valid = valid & main_mask;
+                    if ((valid & main_mask) != main_mask && p.bad_index != nullptr)
+                        *p.bad_index = 1;
+                }
+                __syncwarp();
+            }
             if (lane == 0)
                 mbar_arrive_expect_tx(full, slot_bytes * __popc(valid));
+            const uint32_t dst = stage0 + static_cast<uint32_t>(s) * stage_bytes;
             for (int j = 0; j < n_slots; ++j) {
                 const void *sj = reinterpret_cast<const void *>(
                     __shfl_sync(0xFFFFFFFFu, reinterpret_cast<unsigned long long>(src), j));
                 if (lane == 0 && sj != nullptr)
-                    bulk_g2s(stage0 + s * stage_bytes + j * slot_bytes, sj, slot_bytes, full);
+                    bulk_g2s(dst + j * slot_bytes, sj, slot_bytes, full);
             }
             row = next_row(p, row + gridDim.x);
-            if (kMode == kMoe && lane < n_main && row < rows)
+            if (kMode == kMoe && lane < n_main && row < rows) {
                 e_next = __ldg(idx + row * topk + lane);
+                w_next = __ldg(p.w + row * topk + lane);
+            }
+            if (++s == ns) {
+                s = 0;
+                ++k;
+            }
         }
         if (!ok && lane == 0) {
             atomicOr(&g_device_error, kDeviceErrTimeout);
@@ -397,31 +429,6 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
         }
         const uint32_t k = phase;
 
-        // MoE: routing weights and index validity of this row (broadcast loads,
-        // issued before the wait so that their latency hides behind it)
-        float wj[kMode == kMoe ? LB_MAX_TOPK : 1];
-        bool okj[kMode == kMoe ? LB_MAX_TOPK : 1];
-        if (kMode == kMoe) {
-#pragma unroll
-            for (int j = 0; j < LB_MAX_TOPK; ++j) {
-                okj[j] = false;
-                wj[j] = 0.0f;
-                if (j < p.topk) {
-                    const int32_t e = __ldg(p.idx + row * p.topk + j);
-                    okj[j] = (e >= 0) & (static_cast<int64_t>(e) < p.n_expert_rows);
-                    wj[j] = __ldg(p.w + row * p.topk + j);
-                }
-            }
-            if (p.bad_index != nullptr && ct == 0) {
-                bool bad = false;
-#pragma unroll
-                for (int j = 0; j < LB_MAX_TOPK; ++j)
-                    bad |= (j < p.topk) & !okj[j];
-                if (bad)
-                    *p.bad_index = 1;
-            }
-        }
-
         // A thread whose wait fails reads nothing from the stage and writes nothing;
         // the group learns of it at its row barrier and leaves together.
         const bool ok = mbar_wait_bounded(full0 + 8 * s, k & 1u, &abort_flag);
@@ -436,12 +443,14 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
                 acc[v][e] = make_float2(0.0f, 0.0f);
         if (ok) {
             const uint32_t stage = stage0 + static_cast<uint32_t>(s) * stage_bytes;
+            const uint32_t valid = (kMode == kMoe) ? meta[s].valid : 0u;
 #pragma unroll
             for (int j = 0; j < LB_MAX_K; ++j) {
                 if (j >= n_main)
                     break;
-                if (kMode == kMoe && !okj[j])
+                if (kMode == kMoe && !((valid >> j) & 1u))
                     continue;
+                const float wj = (kMode == kMoe) ? meta[s].w[j] : 1.0f;
                 const uint32_t slot = stage + static_cast<uint32_t>(j) * slot_bytes;
 #pragma unroll
                 for (int v = 0; v < kVpt; ++v)
@@ -450,7 +459,7 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
                         unpack8x2(lds128(slot + soff[v]), f);
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
-                            acc[v][e] = (kMode == kMoe) ? add_mul2_rn(acc[v][e], wj[j], f[e])
+                            acc[v][e] = (kMode == kMoe) ? add_mul2_rn(acc[v][e], wj, f[e])
                                                         : __fadd2_rn(acc[v][e], f[e]);
                     }
             }
