@@ -243,7 +243,11 @@ namespace lb {
 bool use_stream_kernel(int64_t rows, int num_sms) {
     // Enough rows for one persistent CTA per SM; fewer rows go to the row kernel,
     // which splits each row over a cluster to fill the GPU.
+#ifdef LB_STREAM_MIN_ROWS
+    return rows >= LB_STREAM_MIN_ROWS;
+#else
     return rows >= num_sms;
+#endif
 }
 
 bool choose_stream_shape(int64_t rows, int64_t H, int n_inputs, int num_sms,
@@ -301,14 +305,18 @@ bool choose_shape(int64_t rows, int64_t H, int num_sms, Shape *out) {
     if (rows < 0 || H <= 0 || H % 8 != 0 || num_sms <= 0)
         return false;
     const int64_t nvec = H / 8;
-    // Split rows across a cluster while the rows alone would leave the GPU under two
-    // CTAs per SM, keeping at least 64 vectors (two warps) per CTA.
+    // One CTA per row: splitting short rows over a cluster measured slower at decode
+    // sizes (cluster scheduling and barriers cost more than the extra SMs give).
     int cs = 1;
-    while (cs < 8 && rows * cs < 2 * static_cast<int64_t>(num_sms) && nvec / (2 * cs) >= 64)
-        cs *= 2;
-    // Long rows: at most 512 threads x 4 vectors per CTA.
+    (void)rows;
+    (void)num_sms;
+    // Long rows: at most 512 threads x 4 vectors per CTA, else a cluster splits them.
     while (cs < 8 && (nvec + cs - 1) / cs > 2048)
         cs *= 2;
+#ifdef LB_ROW_FORCE_CLUSTER
+    if (nvec % LB_ROW_FORCE_CLUSTER == 0)
+        cs = LB_ROW_FORCE_CLUSTER;
+#endif
     const int64_t vpc = (nvec + cs - 1) / cs;
     if (vpc > 2048)
         return false;

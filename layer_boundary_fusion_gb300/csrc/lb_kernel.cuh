@@ -1,21 +1,18 @@
-// Fused layer-boundary kernel for sm_103a.
+// Row kernel for sm_103a: the boundary for calls with fewer rows than SMs (decode).
 //
-// One token row per CTA, or per thread-block cluster of up to 8 CTAs when there are
-// too few rows to fill the GPU (each CTA then owns a contiguous column range and the
-// row's reductions are combined through distributed shared memory).  Each thread
-// owns whole 16-byte vectors (8 bf16) of the row and makes exactly one pass over
-// HBM:
-//   1. issue the residual load and every partial (or gathered expert-row) load of a
-//      chunk before consuming any, so that (chunk + 1) x 16 B are in flight per
-//      vector;
-//   2. accumulate in binary32 in a fixed order (+0, then k or j ascending, then the
-//      residual) -- the order of the binary32 definition, so residual' is
-//      bit-identical to it;
-//   3. store residual' and the thread's share of sum(o^2) in the same pass;
-//   4. reduce sum(o^2) over the row (warp shuffles, shared memory across warps,
-//      DSMEM across the cluster), r = 1/sqrt(ss/H + eps) with IEEE sqrt and divide;
-//   5. store y = bf16((o*r)*gamma) from registers, and for the FP8 read reduce
-//      max|yf| the same way and store E4M3 codes and the per-token scale.
+// One CTA per token row (a thread-block cluster of up to 8 CTAs splits only rows too
+// long for one CTA, with the row's reduction combined through distributed shared
+// memory).  Each thread owns whole 16-byte vectors (8 bf16) of the row and makes one
+// pass over HBM:
+//   1. issue the residual, gamma and every partial (or gathered expert-row) load of
+//      a chunk -- all of a decode boundary's K <= 8 partials -- before consuming any;
+//   2. accumulate in binary32 pairs (packed f32x2, rounding each lane like the scalar
+//      ops) in a fixed order: +0, then k or j ascending, then the residual -- the
+//      order of the definition, so residual' is bit-identical to it;
+//   3. store residual', and reduce sum(o^2) (and max|o*gamma| for the FP8 read) over
+//      the row in one warp-shuffle + shared-memory step;
+//   4. r = rsqrt(sum/H + eps); store y = bf16((o*r)*gamma), or the E4M3 codes and the
+//      per-token scale with amax = r * max|o*gamma|.
 // Nothing is re-read and nothing is staged in global memory.  Launches are
 // programmatic dependents of the previous kernel in the stream: the launch overlaps
 // its tail, and every global access waits for it (griddepcontrol.wait).
@@ -23,8 +20,7 @@
 // Sources: "Layer boundaries" (sglang developer guide), sections "Residual stream"
 // and "Residual update and input read" (fused add+norm, FP32 accumulation);
 // "SGLang flashinfer_allreduce_fusion精读", section forward (AR + add + RMSNorm as
-// one kernel).  The GB300 design (register-resident rows, cluster split for small
-// batches, no cross-GPU workspace) is this library's own.
+// one kernel).  The GB300 design is this library's own.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -55,13 +51,6 @@ __device__ __forceinline__ uint4 ld_residual(const void *ptr) {
     return *reinterpret_cast<const uint4 *>(ptr);
 }
 
-__device__ __forceinline__ void ld_gamma8(const float *g, float out[8]) {
-    const float4 a = __ldg(reinterpret_cast<const float4 *>(g));
-    const float4 b = __ldg(reinterpret_cast<const float4 *>(g) + 1);
-    out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;
-    out[4] = b.x; out[5] = b.y; out[6] = b.z; out[7] = b.w;
-}
-
 // ------------------------------------------------------------------------------------
 // Programmatic dependent launch
 // ------------------------------------------------------------------------------------
@@ -83,22 +72,48 @@ __device__ __forceinline__ void pdl_wait() {
 // Number formats
 // ------------------------------------------------------------------------------------
 
-// 8 bf16 (element 0 in the low half of .x) -> 8 floats; widening is exact.
-__device__ __forceinline__ void unpack8(const uint4 &v, float f[8]) {
-    f[0] = __uint_as_float(v.x << 16); f[1] = __uint_as_float(v.x & 0xFFFF0000u);
-    f[2] = __uint_as_float(v.y << 16); f[3] = __uint_as_float(v.y & 0xFFFF0000u);
-    f[4] = __uint_as_float(v.z << 16); f[5] = __uint_as_float(v.z & 0xFFFF0000u);
-    f[6] = __uint_as_float(v.w << 16); f[7] = __uint_as_float(v.w & 0xFFFF0000u);
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);   // round to nearest even
     return *reinterpret_cast<uint32_t *>(&b);
 }
 
-__device__ __forceinline__ uint4 pack8(const float f[8]) {
-    return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
-                      pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+// 8 bf16 (element 0 in the low half of .x) -> 4 binary32 pairs; widening is exact.
+__device__ __forceinline__ void unpack8x2(const uint4 &w, float2 f[4]) {
+    f[0] = make_float2(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u));
+    f[1] = make_float2(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
+    f[2] = make_float2(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xFFFF0000u));
+    f[3] = make_float2(__uint_as_float(w.w << 16), __uint_as_float(w.w & 0xFFFF0000u));
+}
+
+__device__ __forceinline__ uint4 pack8x2(const float2 f[4]) {
+    return make_uint4(pack_bf16x2(f[0].x, f[0].y), pack_bf16x2(f[1].x, f[1].y),
+                      pack_bf16x2(f[2].x, f[2].y), pack_bf16x2(f[3].x, f[3].y));
+}
+
+// acc + w * f with the product rounded to binary32 before the add, per lane (the
+// MoE finalize's definition).  ptxas turns a packed f32x2 multiply feeding a packed
+// add into a packed fused multiply-add even when both carry .rn, so the two
+// products are formed with scalar mul.rn.f32 (never fused) and only the add is
+// packed; the parity tests check residual' bit for bit against the definition.
+__device__ __forceinline__ float2 add_mul2_rn(float2 acc, float w, float2 f) {
+    float2 r;
+    asm("{\n\t.reg .b64 a, t;\n\t.reg .f32 px, py;\n\t"
+        "mul.rn.f32 px, %4, %5;\n\t"
+        "mul.rn.f32 py, %4, %6;\n\t"
+        "mov.b64 a, {%2, %3};\n\t"
+        "mov.b64 t, {px, py};\n\t"
+        "add.rn.f32x2 t, a, t;\n\t"
+        "mov.b64 {%0, %1}, t;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(acc.x), "f"(acc.y), "f"(w), "f"(f.x), "f"(f.y));
+    return r;
+}
+
+// Maximum over the warp of a non-negative float (one redux instruction).
+__device__ __forceinline__ float warp_max(float v) {
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
 }
 
 // Two floats -> two E4M3 codes (round to nearest even, saturate to +-448); the first
@@ -112,28 +127,6 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
 // ------------------------------------------------------------------------------------
 // Reductions
 // ------------------------------------------------------------------------------------
-
-template <bool kMax>
-__device__ __forceinline__ float combine(float a, float b) {
-    return kMax ? fmaxf(a, b) : a + b;
-}
-
-// Every thread of the CTA returns the same value.  `red` holds one slot per warp;
-// each call site owns its own array, so no slot is reused within a launch.
-template <bool kMax>
-__device__ __forceinline__ float block_reduce(float v, float *red) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-        v = combine<kMax>(v, __shfl_xor_sync(0xFFFFFFFFu, v, off));
-    if ((threadIdx.x & 31) == 0)
-        red[threadIdx.x >> 5] = v;
-    __syncthreads();
-    const int nwarps = blockDim.x >> 5;
-    float r = red[0];
-    for (int i = 1; i < nwarps; ++i)
-        r = combine<kMax>(r, red[i]);
-    return r;
-}
 
 __device__ __forceinline__ int cluster_size() {
     uint32_t n;
@@ -155,54 +148,24 @@ __device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Combines one value per CTA across the cluster (same value in every thread of a
-// CTA).  Every CTA reads the slots in rank order, so all CTAs get the same result.
-template <bool kMax>
-__device__ __forceinline__ float cluster_reduce(float v, float *slot, int cs) {
-    if (threadIdx.x == 0)
-        *slot = v;
-    cluster_arrive();
-    cluster_wait();
-    const uint32_t local = static_cast<uint32_t>(__cvta_generic_to_shared(slot));
-    float r = 0.0f;
-    for (int c = 0; c < cs; ++c) {
-        uint32_t remote;
-        float x;
-        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(c));
-        asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(x) : "r"(remote) : "memory");
-        r = (c == 0) ? x : combine<kMax>(r, x);
-    }
-    return r;
-}
-
 // ------------------------------------------------------------------------------------
 // The kernel
 // ------------------------------------------------------------------------------------
 
-// Loads in flight per vector: the residual plus a chunk of kChunk partials.
+// Loads in flight per vector: the residual, gamma and a chunk of up to kChunk
+// partials (every partial of a decode boundary, K <= 8, in one batch).
 template <int kVpt>
 struct Chunk {
-    static constexpr int value = (kVpt >= 4) ? 2 : 4;
-};
-
-// At most 512 threads per CTA; one-vector threads are held to 64 registers so that two
-// 512-thread CTAs fit on an SM, wider threads get room for their extra vectors.
-template <int kVpt>
-struct MinBlocks {
-    static constexpr int value = (kVpt == 1) ? 2 : 1;
+    static constexpr int value = (kVpt >= 4) ? 2 : (kVpt == 2 ? 4 : 8);
 };
 
 template <int kMode, bool kFp8, int kVpt>
-__global__ void __launch_bounds__(512, MinBlocks<kVpt>::value)
-    boundary_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(512, 1) boundary_kernel(const __grid_constant__ Params p) {
     constexpr int kChunk = Chunk<kVpt>::value;
-    __shared__ float red_ss[32];
-    __shared__ float red_mx[32];
-    __shared__ float cl_ss;
-    __shared__ float cl_mx;
+    __shared__ __align__(16) float2 red[16];       // one (sum o^2, max|o*gamma|) per warp
+    __shared__ __align__(8) float2 cl_red;         // this CTA's share, for the cluster
 
     pdl_launch_dependents();
-    pdl_wait();
     const int cs = cluster_size();                 // 1 without a cluster launch
     const int crank = (cs > 1) ? cluster_rank() : 0;
     const int64_t row = blockIdx.x / cs;           // all CTAs of a cluster share it
@@ -230,8 +193,11 @@ __global__ void __launch_bounds__(512, MinBlocks<kVpt>::value)
         act[i] = v < vend;
         col[i] = v * 8;
     }
-
     const bool has_res = p.residual_in != nullptr;
+    const bool need_read = kFp8 || p.y_out != nullptr;
+    pdl_wait();                                    // every global access comes after this
+
+    // Residual and gamma loads go out with the first chunk of partials.
     uint4 rv[kVpt];
     if (has_res) {
 #pragma unroll
@@ -239,16 +205,33 @@ __global__ void __launch_bounds__(512, MinBlocks<kVpt>::value)
             if (act[i])
                 rv[i] = ld_residual(p.residual_in + row * H + col[i]);
     }
+    float2 gm[kVpt][4];
+#pragma unroll
+    for (int i = 0; i < kVpt; ++i) {
+        if (act[i] && need_read) {
+            const float4 a = __ldg(reinterpret_cast<const float4 *>(p.gamma + col[i]));
+            const float4 b = __ldg(reinterpret_cast<const float4 *>(p.gamma + col[i]) + 1);
+            gm[i][0] = make_float2(a.x, a.y);
+            gm[i][1] = make_float2(a.z, a.w);
+            gm[i][2] = make_float2(b.x, b.y);
+            gm[i][3] = make_float2(b.z, b.w);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                gm[i][e] = make_float2(0.0f, 0.0f);
+        }
+    }
 
-    float acc[kVpt][8];
+    // o in binary32 pairs, summed in the definition's order (packed adds round each
+    // lane like the scalar ones)
+    float2 acc[kVpt][4];
 #pragma unroll
     for (int i = 0; i < kVpt; ++i)
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-            acc[i][e] = 0.0f;
+        for (int e = 0; e < 4; ++e)
+            acc[i][e] = make_float2(0.0f, 0.0f);
 
     if (kMode == kFold) {
-        // o = +0 + p_0 + p_1 + ... (k ascending)
         const int64_t base = g * H;
         for (int k0 = 0; k0 < p.K; k0 += kChunk) {
             uint4 buf[kChunk][kVpt];
@@ -267,16 +250,17 @@ __global__ void __launch_bounds__(512, MinBlocks<kVpt>::value)
 #pragma unroll
                     for (int i = 0; i < kVpt; ++i)
                         if (act[i]) {
-                            float f[8];
-                            unpack8(buf[kk][i], f);
+                            float2 f[4];
+                            unpack8x2(buf[kk][i], f);
 #pragma unroll
-                            for (int e = 0; e < 8; ++e)
-                                acc[i][e] = __fadd_rn(acc[i][e], f[e]);
+                            for (int e = 0; e < 4; ++e)
+                                acc[i][e] = __fadd2_rn(acc[i][e], f[e]);
                         }
                 }
         }
     } else {
-        // o = +0 + w_0 * E[idx_0] + w_1 * E[idx_1] + ... (j ascending, no FMA)
+        // o = +0 + w_0 * E[idx_0] + w_1 * E[idx_1] + ... (j ascending, each product
+        // rounded before its add)
         const int64_t tk = row * p.topk;
         for (int j0 = 0; j0 < p.topk; j0 += kChunk) {
             uint4 buf[kChunk][kVpt];
@@ -307,11 +291,11 @@ __global__ void __launch_bounds__(512, MinBlocks<kVpt>::value)
 #pragma unroll
                     for (int i = 0; i < kVpt; ++i)
                         if (act[i]) {
-                            float f[8];
-                            unpack8(buf[jj][i], f);
+                            float2 f[4];
+                            unpack8x2(buf[jj][i], f);
 #pragma unroll
-                            for (int e = 0; e < 8; ++e)
-                                acc[i][e] = __fadd_rn(acc[i][e], __fmul_rn(wj[jj], f[e]));
+                            for (int e = 0; e < 4; ++e)
+                                acc[i][e] = add_mul2_rn(acc[i][e], wj[jj], f[e]);
                         }
                 }
         }
@@ -322,98 +306,117 @@ __global__ void __launch_bounds__(512, MinBlocks<kVpt>::value)
 #pragma unroll
         for (int i = 0; i < kVpt; ++i)
             if (act[i]) {
-                float f[8];
-                unpack8(rv[i], f);
+                float2 f[4];
+                unpack8x2(rv[i], f);
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    acc[i][e] = __fadd_rn(acc[i][e], f[e]);
+                for (int e = 0; e < 4; ++e)
+                    acc[i][e] = __fadd2_rn(acc[i][e], f[e]);
             }
     }
     if (p.residual_out != nullptr) {
 #pragma unroll
         for (int i = 0; i < kVpt; ++i)
             if (act[i])
-                *reinterpret_cast<uint4 *>(p.residual_out + row * H + col[i]) = pack8(acc[i]);
+                *reinterpret_cast<uint4 *>(p.residual_out + row * H + col[i]) = pack8x2(acc[i]);
     }
-
-    if (!kFp8 && p.y_out == nullptr)
+    if (!need_read)
         return;                                    // complete_output / fold only
 
-    // gamma is re-read by every row: cached loads, issued before the reduction.
-    float gm[kVpt][8];
-#pragma unroll
-    for (int i = 0; i < kVpt; ++i)
-        if (act[i])
-            ld_gamma8(p.gamma + col[i], gm[i]);
-
-    // r = 1 / sqrt(mean(o^2) + eps) over the whole row
-    float ss = 0.0f;
+    // One reduction for the row: sum(o^2) and, for FP8, max|o * gamma| (the read's
+    // amax is r * max|o * gamma| since r > 0).
+    float2 ss2 = make_float2(0.0f, 0.0f);
+    float mg = 0.0f;
 #pragma unroll
     for (int i = 0; i < kVpt; ++i)
         if (act[i])
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-                ss = __fmaf_rn(acc[i][e], acc[i][e], ss);
-    ss = block_reduce<false>(ss, red_ss);
-    if (cs > 1)
-        ss = cluster_reduce<false>(ss, &cl_ss, cs);
-    const float r = 1.0f / sqrtf(ss / static_cast<float>(H) + p.eps);
+            for (int e = 0; e < 4; ++e) {
+                ss2 = __ffma2_rn(acc[i][e], acc[i][e], ss2);
+                if (kFp8) {
+                    const float2 t = __fmul2_rn(acc[i][e], gm[i][e]);
+                    mg = fmaxf(mg, fmaxf(fabsf(t.x), fabsf(t.y)));
+                }
+            }
+    float ss = ss2.x + ss2.y;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        ss += __shfl_xor_sync(0xFFFFFFFFu, ss, off);
+    if (kFp8)
+        mg = warp_max(mg);
+    if ((threadIdx.x & 31) == 0)
+        red[threadIdx.x >> 5] = make_float2(ss, mg);
+    __syncthreads();
+    const int nwarps = blockDim.x >> 5;
+    ss = 0.0f;
+    mg = 0.0f;
+    for (int w = 0; w < nwarps; ++w) {
+        const float2 t = red[w];
+        ss += t.x;
+        mg = fmaxf(mg, t.y);
+    }
+    if (cs > 1) {
+        // across the cluster (long rows): every CTA sums the CTAs' shares in rank order
+        if (threadIdx.x == 0)
+            cl_red = make_float2(ss, mg);
+        cluster_arrive();
+        cluster_wait();
+        const uint32_t local = static_cast<uint32_t>(__cvta_generic_to_shared(&cl_red));
+        ss = 0.0f;
+        mg = 0.0f;
+        for (int c = 0; c < cs; ++c) {
+            uint32_t remote;
+            float x, y;
+            asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(c));
+            asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];"
+                         : "=f"(x), "=f"(y)
+                         : "r"(remote)
+                         : "memory");
+            ss += x;
+            mg = fmaxf(mg, y);
+        }
+        cluster_arrive();                          // done with the peers' shares
+    }
+    const float r = rsqrtf(__fmaf_rn(ss, p.inv_H, p.eps));
+    const float2 r2 = make_float2(r, r);
 
     // yf = (o * r) * gamma
 #pragma unroll
     for (int i = 0; i < kVpt; ++i)
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-            acc[i][e] = __fmul_rn(__fmul_rn(acc[i][e], r), act[i] ? gm[i][e] : 0.0f);
+        for (int e = 0; e < 4; ++e)
+            acc[i][e] = __fmul2_rn(__fmul2_rn(acc[i][e], r2), gm[i][e]);
 
-    if (!kFp8) {
-        if (cs > 1)
-            cluster_arrive();                      // done with the peers' slots
-#pragma unroll
-        for (int i = 0; i < kVpt; ++i)
-            if (act[i])
-                *reinterpret_cast<uint4 *>(p.y_out + row * H + col[i]) = pack8(acc[i]);
-        if (cs > 1)
-            cluster_wait();                        // keep our slot alive for them
-        return;
-    }
-
-    // FP8 read: scale = max|yf| / 448, q = E4M3(yf * 448 / max|yf|)
-    float mx = 0.0f;
-#pragma unroll
-    for (int i = 0; i < kVpt; ++i)
-        if (act[i])
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                mx = fmaxf(mx, fabsf(acc[i][e]));
-    mx = block_reduce<true>(mx, red_mx);
-    if (cs > 1) {
-        mx = cluster_reduce<true>(mx, &cl_mx, cs);
-        cluster_arrive();
-    }
     if (p.y_out != nullptr) {
 #pragma unroll
         for (int i = 0; i < kVpt; ++i)
             if (act[i])
-                *reinterpret_cast<uint4 *>(p.y_out + row * H + col[i]) = pack8(acc[i]);
+                *reinterpret_cast<uint4 *>(p.y_out + row * H + col[i]) = pack8x2(acc[i]);
     }
-    const bool nonzero = mx > 0.0f;
-    const float inv = nonzero ? 448.0f / mx : 0.0f;
-    if (threadIdx.x == 0 && crank == 0)
-        p.scale_out[row] = mx / 448.0f;
+    if (kFp8) {
+        // FP8 read: scale = amax / 448, q = E4M3(yf * 448 / amax); an all-zero row gets
+        // scale 0 and codes 0x00.
+        const float amax = __fmul_rn(r, mg);
+        if (threadIdx.x == 0 && crank == 0)
+            p.scale_out[row] = amax / 448.0f;
+        const float inv = amax > 0.0f ? __fdividef(448.0f, amax) : 0.0f;
+        const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
-    for (int i = 0; i < kVpt; ++i)
-        if (act[i]) {
-            float v[8];
+        for (int i = 0; i < kVpt; ++i)
+            if (act[i]) {
+                uint2 out = make_uint2(0u, 0u);
+                if (amax > 0.0f) {
+                    float2 q[4];
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-                v[e] = nonzero ? __fmul_rn(acc[i][e], inv) : 0.0f;
-            const uint32_t lo = cvt_e4m3x2(v[0], v[1]) | (cvt_e4m3x2(v[2], v[3]) << 16);
-            const uint32_t hi = cvt_e4m3x2(v[4], v[5]) | (cvt_e4m3x2(v[6], v[7]) << 16);
-            *reinterpret_cast<uint2 *>(p.q_out + row * H + col[i]) = make_uint2(lo, hi);
-        }
+                    for (int e = 0; e < 4; ++e)
+                        q[e] = __fmul2_rn(acc[i][e], inv2);
+                    out.x = cvt_e4m3x2(q[0].x, q[0].y) | (cvt_e4m3x2(q[1].x, q[1].y) << 16);
+                    out.y = cvt_e4m3x2(q[2].x, q[2].y) | (cvt_e4m3x2(q[3].x, q[3].y) << 16);
+                }
+                *reinterpret_cast<uint2 *>(p.q_out + row * H + col[i]) = out;
+            }
+    }
     if (cs > 1)
-        cluster_wait();
+        cluster_wait();                            // keep our share alive for the peers
 }
 
 // ------------------------------------------------------------------------------------

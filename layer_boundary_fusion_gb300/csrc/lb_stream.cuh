@@ -116,38 +116,6 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     return v;
 }
 
-// 8 bf16 (element 0 in the low half of .x) -> 4 binary32 pairs; widening is exact.
-__device__ __forceinline__ void unpack8x2(const uint4 &w, float2 f[4]) {
-    f[0] = make_float2(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u));
-    f[1] = make_float2(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
-    f[2] = make_float2(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xFFFF0000u));
-    f[3] = make_float2(__uint_as_float(w.w << 16), __uint_as_float(w.w & 0xFFFF0000u));
-}
-
-__device__ __forceinline__ uint4 pack8x2(const float2 f[4]) {
-    return make_uint4(pack_bf16x2(f[0].x, f[0].y), pack_bf16x2(f[1].x, f[1].y),
-                      pack_bf16x2(f[2].x, f[2].y), pack_bf16x2(f[3].x, f[3].y));
-}
-
-// acc + w * f with the product rounded to binary32 before the add, per lane (the
-// MoE finalize's definition).  ptxas turns a packed f32x2 multiply feeding a packed
-// add into a packed fused multiply-add even when both carry .rn, so the two
-// products are formed with scalar mul.rn.f32 (never fused) and only the add is
-// packed; the parity tests check residual' bit for bit against the definition.
-__device__ __forceinline__ float2 add_mul2_rn(float2 acc, float w, float2 f) {
-    float2 r;
-    asm("{\n\t.reg .b64 a, t;\n\t.reg .f32 px, py;\n\t"
-        "mul.rn.f32 px, %4, %5;\n\t"
-        "mul.rn.f32 py, %4, %6;\n\t"
-        "mov.b64 a, {%2, %3};\n\t"
-        "mov.b64 t, {px, py};\n\t"
-        "add.rn.f32x2 t, a, t;\n\t"
-        "mov.b64 {%0, %1}, t;\n\t}"
-        : "=f"(r.x), "=f"(r.y)
-        : "f"(acc.x), "f"(acc.y), "f"(w), "f"(f.x), "f"(f.y));
-    return r;
-}
-
 // One bulk copy global -> this CTA's shared memory, completing on `bar`.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
                                          uint32_t bar) {
@@ -207,13 +175,6 @@ struct StreamThreads {
 };
 constexpr int kGroupsMax =
     LB_STREAM_GROUPS > LB_STREAM_GROUPS_WIDE ? LB_STREAM_GROUPS : LB_STREAM_GROUPS_WIDE;
-
-// Maximum over the warp of a non-negative float (one redux instruction).
-__device__ __forceinline__ float warp_max(float v) {
-    float r;
-    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
-    return r;
-}
 
 // Group-local barrier that also ORs a predicate over the group (barrier id 1 + g).
 __device__ __forceinline__ bool group_sync_or(bool pred, int id, int nthreads) {

@@ -70,8 +70,8 @@ SMEM = 232448          # opt-in shared memory per CTA on GB300
     (2048, 4096, 5, (1, 152, 800, 2, 1, 3, 123168)),    # prefill K=4 + residual: stream
     (1024, 4096, 9, (1, 152, 800, 2, 1, 3, 221472)),    # MoE top-8 + residual: stream
     (254, 4096, 9, (1, 152, 800, 2, 1, 3, 221472)),     # one ragged slice: stream
-    (64, 4096, 9, (0, 512, 64, 1, 8, 0, 0)),            # decode: 8-CTA clusters per row
-    (1, 4096, 2, (0, 8, 64, 1, 8, 0, 0)),
+    (64, 4096, 9, (0, 64, 512, 1, 1, 0, 0)),            # decode: row kernel, a CTA per row
+    (1, 4096, 2, (0, 1, 512, 1, 1, 0, 0)),
     (16, 512, 3, (0, 16, 64, 1, 1, 0, 0)),              # tiny: one CTA per row
     (4096, 8192, 5, (1, 152, 288, 4, 1, 2, 164032)),
     (4096, 8192, 9, (0, 4096, 512, 2, 1, 0, 0)),        # no double-buffered stage fits

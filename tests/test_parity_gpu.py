@@ -362,7 +362,8 @@ def test_specified_workloads_take_the_intended_kernels(lb):
     assert plan(lb, 1024, 4096, 9).kernel == lb.LB_KERNEL_STREAM     # MoE finalize
     assert plan(lb, 254, 4096, 9).kernel == lb.LB_KERNEL_STREAM      # ragged slice
     p = plan(lb, 64, 4096, 9)                                        # decode
-    assert p.kernel == lb.LB_KERNEL_ROW and p.ctas_per_row > 1
+    assert p.kernel == lb.LB_KERNEL_ROW and p.grid == 64
+    assert plan(lb, 4, 32768, 2).ctas_per_row == 2                   # long rows: cluster
 
 
 # --------------------------------------------------------------------------------------
@@ -372,14 +373,16 @@ def test_specified_workloads_take_the_intended_kernels(lb):
 @pytest.mark.parametrize("K,T,H", [
     (1, 1, 8),          # a single vector per row
     (3, 5, 520),        # 65 vectors: partly active warp
-    (16, 3, 4096),      # maximum K; 8-CTA clusters
-    (2, 33, 8192),      # two vectors per thread, cluster split
+    (16, 3, 4096),      # maximum K, two load chunks
+    (2, 33, 8192),      # two vectors per thread, row kernel
     (2, 400, 8192),     # two vectors per thread, no cluster
     (2, 9, 16384),      # four vectors per thread
-    (1, 4, 32768),      # four vectors per thread, two-CTA clusters
+    (1, 4, 32768),      # four vectors per thread, a row split over a 2-CTA cluster
     (5, 301, 4096),     # K above one load chunk, ragged last wave
     (4, 2048, 1024),
     (8, 152, 2048),
+    (2, 160, 4096),     # stream kernel, one or two rows per CTA
+    (4, 1000, 4096),    # stream kernel
 ])
 def test_shapes(lb, K, T, H):
     w = wl.fold_workload("shape", K, T, H, seed=K * 1000 + T + H)
