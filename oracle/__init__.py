@@ -32,18 +32,22 @@ def _load():
         lib = ctypes.CDLL(path)
         vp = ctypes.c_void_p
         i64 = ctypes.c_int64
-        lib.ora_fold_norm.argtypes = [ctypes.POINTER(vp), ctypes.c_int, vp, vp, i64, i64,
+        ci = ctypes.c_int
+        lib.ora_fold_norm.argtypes = [ctypes.POINTER(vp), ci, vp, vp, ci, i64, i64,
                                       ctypes.c_float, vp, vp, vp, vp, vp]
         lib.ora_fold_norm.restype = ctypes.c_int
-        lib.ora_moe_finalize_fold_norm.argtypes = [vp, i64, vp, vp, ctypes.c_int, vp, vp,
+        lib.ora_moe_finalize_fold_norm.argtypes = [vp, i64, vp, vp, ci, vp, vp, ci,
                                                    i64, i64, ctypes.c_float, vp, vp, vp,
                                                    vp, vp]
         lib.ora_moe_finalize_fold_norm.restype = ctypes.c_int
-        lib.ora_slice_fold_norm.argtypes = [ctypes.POINTER(vp), ctypes.c_int, i64,
-                                            ctypes.c_int, ctypes.c_int, vp, vp,
-                                            ctypes.c_int, vp, vp, i64, ctypes.c_float,
+        lib.ora_slice_fold_norm.argtypes = [ctypes.POINTER(vp), ci, i64, ci, ci, vp, vp,
+                                            ci, vp, vp, ci, i64, ctypes.c_float,
                                             vp, vp, vp, vp, vp]
         lib.ora_slice_fold_norm.restype = ctypes.c_int64
+        lib.ora_set_slice_fold_norm.argtypes = [ctypes.POINTER(vp), ci, i64, ci, vp, vp, ci,
+                                                vp, vp, ci, i64, ctypes.c_float, vp, vp, vp,
+                                                vp, vp]
+        lib.ora_set_slice_fold_norm.restype = ctypes.c_int64
         for name in ("ora_bf16_to_f32_array", "ora_f32_to_bf16_array",
                      "ora_f32_to_e4m3_array", "ora_e4m3_to_f32_array"):
             getattr(lib, name).argtypes = [vp, vp, i64]
@@ -116,11 +120,12 @@ def _outputs(shape_rows, H, want_residual, want_y, want_fp8, out=None):
 
 
 def fold_norm(partials, residual_in, gamma, eps, *, want_residual=True, want_y=True,
-              want_fp8=False, out=None):
+              want_fp8=False, out=None, gemma=False):
     """Complete the owed sum of K partials, fold it into the residual, then read.
 
     o = (sum_k partials[k], k ascending, from +0) + residual_in (absent if None);
-    residual_out = bf16(o); y = bf16(RMSNorm(o) * gamma); FP8: q, scale per token.
+    residual_out = bf16(o); y = bf16(RMSNorm(o) * weight) with weight = gamma, or
+    1 + gamma when `gemma`; FP8: q, scale per token.
     Returns a dict with the requested outputs ("residual_out", "y", "q", "scale").
     `out` may supply preallocated outputs (rows not written keep their bytes).
     """
@@ -135,7 +140,8 @@ def fold_norm(partials, residual_in, gamma, eps, *, want_residual=True, want_y=T
     res = _outputs(T, H, want_residual, want_y, want_fp8, out)
     arr = (ctypes.c_void_p * max(1, len(partials)))(*[p.ctypes.data for p in partials])
     work = np.empty(2 * H, np.float32)
-    rc = _load().ora_fold_norm(arr, len(partials), _ptr(residual_in), _ptr(gamma), T, H,
+    rc = _load().ora_fold_norm(arr, len(partials), _ptr(residual_in), _ptr(gamma),
+                               int(gemma), T, H,
                                ctypes.c_float(eps), _ptr(res.get("residual_out")),
                                _ptr(res.get("y")), _ptr(res.get("q")),
                                _ptr(res.get("scale")), _ptr(work))
@@ -145,7 +151,8 @@ def fold_norm(partials, residual_in, gamma, eps, *, want_residual=True, want_y=T
 
 
 def moe_finalize_fold_norm(expert_out, idx, w, residual_in, gamma, eps, *,
-                           want_residual=True, want_y=True, want_fp8=False, out=None):
+                           want_residual=True, want_y=True, want_fp8=False, out=None,
+                           gemma=False):
     """Deferred MoE finalize folded into the residual, then read.
 
     o[t] = sum_j (w[t,j] * expert_out[idx[t,j]]) (j ascending, each product rounded
@@ -164,7 +171,7 @@ def moe_finalize_fold_norm(expert_out, idx, w, residual_in, gamma, eps, *,
     work = np.empty(2 * H, np.float32)
     bad = _load().ora_moe_finalize_fold_norm(
         _ptr(expert_out), n_rows, _ptr(idx), _ptr(w), topk, _ptr(residual_in),
-        _ptr(gamma), T, H, ctypes.c_float(eps), _ptr(res.get("residual_out")),
+        _ptr(gamma), int(gemma), T, H, ctypes.c_float(eps), _ptr(res.get("residual_out")),
         _ptr(res.get("y")), _ptr(res.get("q")), _ptr(res.get("scale")), _ptr(work))
     res["bad_index"] = bool(bad)
     return res
@@ -172,7 +179,7 @@ def moe_finalize_fold_norm(expert_out, idx, w, residual_in, gamma, eps, *,
 
 def slice_fold_norm(partials, T_pad, num_slices, slice_, offsets, counts, residual_in,
                     gamma, eps, *, want_residual=True, want_y=True, want_fp8=False,
-                    out=None):
+                    out=None, gemma=False):
     """Slice `slice_` of a padded ragged batch (fixed-size reduce-scatter completion).
 
     Outputs are compact [S, H] with S = T_pad / num_slices; padding rows are left
@@ -192,11 +199,40 @@ def slice_fold_norm(partials, T_pad, num_slices, slice_, offsets, counts, residu
     work = np.empty(2 * H, np.float32)
     n = _load().ora_slice_fold_norm(
         arr, len(partials), T_pad, num_slices, slice_, _ptr(offsets), _ptr(counts),
-        len(offsets), _ptr(residual_in), _ptr(gamma), H, ctypes.c_float(eps),
+        len(offsets), _ptr(residual_in), _ptr(gamma), int(gemma), H, ctypes.c_float(eps),
         _ptr(res.get("residual_out")), _ptr(res.get("y")), _ptr(res.get("q")),
         _ptr(res.get("scale")), _ptr(work))
     if n < 0:
         raise ValueError("oracle rejected the slice metadata")
+    res["rows_written"] = int(n)
+    return res
+
+
+def set_slice_fold_norm(partials, T_pad, set_, offsets, counts, residual_in, gamma, eps, *,
+                        want_residual=True, want_y=True, want_fp8=False, out=None,
+                        gemma=False):
+    """Rank `set_`'s rows under a variable-size reduce-scatter: the valid rows of
+    token set `set_`, as compact [counts[set_], H] outputs."""
+    partials = [_c(p, np.uint16) for p in partials]
+    H = partials[0].shape[1] if partials else residual_in.shape[1]
+    offsets = _c(np.asarray(offsets, np.int32), np.int32)
+    counts = _c(np.asarray(counts, np.int32), np.int32)
+    if not 0 <= set_ < len(counts):
+        raise ValueError("set index out of range")
+    rows = int(counts[set_])
+    if residual_in is not None:
+        residual_in = _c(residual_in, np.uint16)
+    gamma = None if gamma is None else _c(gamma, np.float32)
+    res = _outputs(rows, H, want_residual, want_y, want_fp8, out)
+    arr = (ctypes.c_void_p * max(1, len(partials)))(*[p.ctypes.data for p in partials])
+    work = np.empty(2 * H, np.float32)
+    n = _load().ora_set_slice_fold_norm(
+        arr, len(partials), T_pad, set_, _ptr(offsets), _ptr(counts), len(offsets),
+        _ptr(residual_in), _ptr(gamma), int(gemma), H, ctypes.c_float(eps),
+        _ptr(res.get("residual_out")), _ptr(res.get("y")), _ptr(res.get("q")),
+        _ptr(res.get("scale")), _ptr(work))
+    if n < 0:
+        raise ValueError("oracle rejected the set metadata")
     res["rows_written"] = int(n)
     return res
 

@@ -137,13 +137,16 @@ uint8_t ora_f32_to_e4m3(float x)
 /* Consumer read: RMSNorm of the FP32 row o[0..H) with weight gamma.
  *   ms = (sum_h o[h]^2) / H            binary64 (exact squares, h order)
  *   r  = (float)(1 / sqrt(ms + eps))   binary64, rounded once to binary32
- *   yf[h] = (o[h] * r) * gamma[h]      binary32
+ *   yf[h] = (o[h] * r) * weight[h]     binary32
+ * weight = gamma, or 1 + gamma (binary32) for the Gemma form of the norm that the
+ * fused final-norm handoff expects ("Layer boundaries", section "Enter and leave the
+ * layer stack": the fused path reads a GemmaRMSNorm's weight).
  * The pages fix FP32 for the accumulated residual o, which is what is normalised;
  * they say nothing about the precision of the norm's own sum of squares, so it is
  * taken in binary64: a sequential binary32 sum over a long row would carry an error
  * growing with H that belongs to no reading of the method. */
-static void rmsnorm_row(const float *o, const float *gamma, int64_t H, float eps,
-                        float *yf)
+static void rmsnorm_row(const float *o, const float *gamma, int gemma, int64_t H,
+                        float eps, float *yf)
 {
     double ss = 0.0;
     for (int64_t h = 0; h < H; ++h) {
@@ -153,8 +156,9 @@ static void rmsnorm_row(const float *o, const float *gamma, int64_t H, float eps
     double ms = ss / (double)H;
     float r = (float)(1.0 / sqrt(ms + (double)eps));
     for (int64_t h = 0; h < H; ++h) {
+        float weight = gemma ? 1.0f + gamma[h] : gamma[h];
         float t = o[h] * r;
-        yf[h] = t * gamma[h];
+        yf[h] = t * weight;
     }
 }
 
@@ -175,7 +179,7 @@ static void quantize_row(const float *yf, int64_t H, uint8_t *q, float *scale)
 }
 
 /* Writes every requested output of one row from its FP32 sum o.  NULL = not wanted. */
-static void emit_row(const float *o, int64_t H, float eps, const float *gamma,
+static void emit_row(const float *o, int64_t H, float eps, const float *gamma, int gemma,
                      uint16_t *res_out, uint16_t *y_out, uint8_t *q_out,
                      float *scale_out, float *yf_buf)
 {
@@ -183,7 +187,7 @@ static void emit_row(const float *o, int64_t H, float eps, const float *gamma,
         for (int64_t h = 0; h < H; ++h)
             res_out[h] = ora_f32_to_bf16(o[h]);
     if (y_out || q_out) {
-        rmsnorm_row(o, gamma, H, eps, yf_buf);
+        rmsnorm_row(o, gamma, gemma, H, eps, yf_buf);
         if (y_out)
             for (int64_t h = 0; h < H; ++h)
                 y_out[h] = ora_f32_to_bf16(yf_buf[h]);
@@ -216,7 +220,7 @@ static void fold_row(const uint16_t *const *prow, int K, const uint16_t *res,
  * res_in: bf16 [T,H] or NULL (Initial); outputs bf16 [T,H] / u8 [T,H] / f32 [T], each
  * NULL when not wanted.  work: caller scratch of 2*H floats.  Returns 0. */
 int ora_fold_norm(const uint16_t *const *partials, int K, const uint16_t *res_in,
-                  const float *gamma, int64_t T, int64_t H, float eps,
+                  const float *gamma, int gemma, int64_t T, int64_t H, float eps,
                   uint16_t *res_out, uint16_t *y_out, uint8_t *q_out,
                   float *scale_out, float *work)
 {
@@ -228,7 +232,7 @@ int ora_fold_norm(const uint16_t *const *partials, int K, const uint16_t *res_in
         for (int k = 0; k < K; ++k)
             prow[k] = partials[k] + t * H;
         fold_row(prow, K, res_in ? res_in + t * H : NULL, H, o);
-        emit_row(o, H, eps, gamma,
+        emit_row(o, H, eps, gamma, gemma,
                  res_out ? res_out + t * H : NULL,
                  y_out ? y_out + t * H : NULL,
                  q_out ? q_out + t * H : NULL,
@@ -244,7 +248,8 @@ int ora_fold_norm(const uint16_t *const *partials, int K, const uint16_t *res_in
  * [0, n_rows) contributes nothing and makes the return value 1. */
 int ora_moe_finalize_fold_norm(const uint16_t *E, int64_t n_rows, const int32_t *idx,
                                const float *w, int topk, const uint16_t *res_in,
-                               const float *gamma, int64_t T, int64_t H, float eps,
+                               const float *gamma, int gemma, int64_t T, int64_t H,
+                               float eps,
                                uint16_t *res_out, uint16_t *y_out, uint8_t *q_out,
                                float *scale_out, float *work)
 {
@@ -266,7 +271,7 @@ int ora_moe_finalize_fold_norm(const uint16_t *E, int64_t n_rows, const int32_t 
                 acc = acc + ora_bf16_to_f32(res_in[t * H + h]);
             o[h] = acc;
         }
-        emit_row(o, H, eps, gamma,
+        emit_row(o, H, eps, gamma, gemma,
                  res_out ? res_out + t * H : NULL,
                  y_out ? y_out + t * H : NULL,
                  q_out ? q_out + t * H : NULL,
@@ -286,8 +291,8 @@ int ora_moe_finalize_fold_norm(const uint16_t *E, int64_t n_rows, const int32_t 
 int64_t ora_slice_fold_norm(const uint16_t *const *partials, int K, int64_t T_pad,
                             int num_slices, int slice, const int32_t *offsets,
                             const int32_t *counts, int num_sets,
-                            const uint16_t *res_in, const float *gamma, int64_t H,
-                            float eps, uint16_t *res_out, uint16_t *y_out,
+                            const uint16_t *res_in, const float *gamma, int gemma,
+                            int64_t H, float eps, uint16_t *res_out, uint16_t *y_out,
                             uint8_t *q_out, float *scale_out, float *work)
 {
     const uint16_t *prow[64];
@@ -308,7 +313,7 @@ int64_t ora_slice_fold_norm(const uint16_t *const *partials, int K, int64_t T_pa
         for (int k = 0; k < K; ++k)
             prow[k] = partials[k] + g * H;
         fold_row(prow, K, res_in ? res_in + i * H : NULL, H, o);
-        emit_row(o, H, eps, gamma,
+        emit_row(o, H, eps, gamma, gemma,
                  res_out ? res_out + i * H : NULL,
                  y_out ? y_out + i * H : NULL,
                  q_out ? q_out + i * H : NULL,
@@ -316,6 +321,38 @@ int64_t ora_slice_fold_norm(const uint16_t *const *partials, int K, int64_t T_pa
         ++written;
     }
     return written;
+}
+
+/* One rank's rows of a padded, ragged batch under a variable-size reduce-scatter
+ * ("Layer boundaries", section "Choose a reduction policy", value rsv; section "Token
+ * layouts and sums": ATTN_DP token sets).  Rank `set` receives exactly the valid rows
+ * of its own token set, [offsets[set], offsets[set] + counts[set]), as compact
+ * [counts[set], ...] arrays; local row i is global row offsets[set] + i.  Returns the
+ * number of rows written, or -1 on bad metadata. */
+int64_t ora_set_slice_fold_norm(const uint16_t *const *partials, int K, int64_t T_pad,
+                                int set, const int32_t *offsets, const int32_t *counts,
+                                int num_sets, const uint16_t *res_in, const float *gamma,
+                                int gemma, int64_t H, float eps, uint16_t *res_out,
+                                uint16_t *y_out, uint8_t *q_out, float *scale_out,
+                                float *work)
+{
+    const uint16_t *prow[64];
+    if (K < 0 || K > 64 || set < 0 || set >= num_sets || counts[set] < 0 ||
+        (int64_t)offsets[set] + counts[set] > T_pad)
+        return -1;
+    float *o = work, *yf = work + H;
+    for (int64_t i = 0; i < counts[set]; ++i) {
+        int64_t g = (int64_t)offsets[set] + i;
+        for (int k = 0; k < K; ++k)
+            prow[k] = partials[k] + g * H;
+        fold_row(prow, K, res_in ? res_in + i * H : NULL, H, o);
+        emit_row(o, H, eps, gamma, gemma,
+                 res_out ? res_out + i * H : NULL,
+                 y_out ? y_out + i * H : NULL,
+                 q_out ? q_out + i * H : NULL,
+                 scale_out ? scale_out + i : NULL, yf);
+    }
+    return counts[set];
 }
 
 /* Elementwise format helpers over arrays, for the tests. */

@@ -409,3 +409,45 @@ def test_slice_rejects_unequal_slices(ora):
     with pytest.raises(ValueError):
         ora.slice_fold_norm(w.partials, w.T_pad, 3, 0, w.set_offsets, w.set_counts,
                             w.residual, w.gamma, w.eps)
+
+
+# --------------------------------------------------------------------------------------
+# Gemma weight (1 + gamma) and variable-size reduce-scatter (rsv)
+# --------------------------------------------------------------------------------------
+
+def test_gemma_weight_on_the_hand_row(ora):
+    """With weight 1 + gamma, passing gamma - 1 must reproduce the plain hand row."""
+    g = _golden_row("fold_norm_h4.txt")
+    p = [bits(g["p0"])[None], bits(g["p1"])[None]]
+    res = bits(g["res"])[None]
+    out = ora.fold_norm(p, res, (g["gamma"] - 1).astype(np.float32), 0.0, gemma=True)
+    assert np.array_equal(f32_of_bits(out["y"][0]), g["y"])
+    assert np.array_equal(f32_of_bits(out["residual_out"][0]), g["residual_out"])
+
+
+def test_gemma_weight_matches_torch_rmsnorm(ora):
+    w = wl.fold_workload("gemma", 2, 30, 640, seed=91, residual=False)
+    small = (0.05 * np.random.default_rng(3).standard_normal(w.H)).astype(np.float32)
+    out = ora.fold_norm([w.partials[0]], None, small, w.eps, gemma=True)
+    x = torch.from_numpy(f32_of_bits(w.partials[0]).astype(np.float64))
+    ref = torch.nn.functional.rms_norm(x, (w.H,), weight=torch.from_numpy(
+        1.0 + small.astype(np.float64)), eps=w.eps).numpy()
+    assert np.all(close_bf16(out["y"], ref, rel=2.0 ** -8 + 1e-6))
+    plain = ora.fold_norm([w.partials[0]], None, small, w.eps)
+    assert not np.array_equal(plain["y"], out["y"])
+
+
+def test_rsv_gives_each_rank_exactly_its_token_set(ora):
+    counts = wl.RAGGED_COUNTS
+    w = wl.slice_workload("rsv", 3, 32, counts, 8, 0, seed=92)
+    full = ora.fold_norm(w.partials, w.residual_full, w.gamma, w.eps, want_fp8=True)
+    for s, (o, c) in enumerate(zip(w.set_offsets, w.set_counts)):
+        res = ora.set_slice_fold_norm(w.partials, w.T_pad, s, w.set_offsets, w.set_counts,
+                                      w.residual_full[o:o + c], w.gamma, w.eps,
+                                      want_fp8=True)
+        assert res["rows_written"] == counts[s] and res["residual_out"].shape[0] == counts[s]
+        for k in ("residual_out", "y", "q", "scale"):
+            assert np.array_equal(res[k], full[k][o:o + c])
+    with pytest.raises(ValueError):
+        ora.set_slice_fold_norm(w.partials, w.T_pad, 4, w.set_offsets, w.set_counts,
+                                None, w.gamma, w.eps)
