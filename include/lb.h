@@ -74,6 +74,23 @@ int lb_last_cuda_error(void);
 /* Library version: major * 10000 + minor * 100 + patch. */
 int lb_version(void);
 
+/*
+ * Optional behaviour of a call; pass NULL for the defaults (plain gamma, no snapshot).
+ *   flags              LB_OPT_GEMMA_WEIGHT: the read's weight is 1 + gamma (the Gemma
+ *                      form of RMSNorm that the fused final-norm handoff reads,
+ *                      "Layer boundaries", section "Enter and leave the layer stack")
+ *   residual_snapshot  bf16 output [rows, H] receiving a second copy of residual'
+ *                      (an owned snapshot of the updated residual, section "Auxiliary
+ *                      capture and extra contributions"), or NULL; 16-byte aligned
+ * An extra contribution added exactly once ("add_to_output") is one more partial.
+ */
+#define LB_OPT_GEMMA_WEIGHT 1u
+
+typedef struct {
+    unsigned int flags;
+    void *residual_snapshot;
+} lb_options;
+
 /* Kernels of the library (lb_plan.kernel). */
 #define LB_KERNEL_ROW 0     /* one CTA, or a cluster of up to 8 CTAs, per token row */
 #define LB_KERNEL_STREAM 1  /* persistent CTAs streaming rows through TMA stages */
@@ -139,7 +156,7 @@ lb_status lb_device_error(unsigned int *flags, int clear);
  */
 lb_status lb_fold_norm(const void *const *partials, int K, const void *residual_in,
                        void *residual_out, const float *gamma, void *y_out, int64_t T,
-                       int64_t H, float eps, lb_stream_t stream);
+                       int64_t H, float eps, const lb_options *options, lb_stream_t stream);
 
 /*
  * lb_fold_norm_fp8 — lb_fold_norm whose read is quantised per token to FP8 E4M3
@@ -154,7 +171,7 @@ lb_status lb_fold_norm(const void *const *partials, int K, const void *residual_
 lb_status lb_fold_norm_fp8(const void *const *partials, int K, const void *residual_in,
                            void *residual_out, const float *gamma, uint8_t *q_out,
                            float *scale_out, void *y_out, int64_t T, int64_t H, float eps,
-                           lb_stream_t stream);
+                           const lb_options *options, lb_stream_t stream);
 
 /*
  * lb_moe_finalize_fold_norm — deferred MoE finalize fused with the fold and read.
@@ -182,7 +199,8 @@ lb_status lb_moe_finalize_fold_norm(const void *expert_out, int64_t n_expert_row
                                     const void *residual_in, void *residual_out,
                                     const float *gamma, void *y_out, uint8_t *q_out,
                                     float *scale_out, int64_t T, int64_t H, float eps,
-                                    int32_t *bad_index_flag, lb_stream_t stream);
+                                    int32_t *bad_index_flag, const lb_options *options,
+                                    lb_stream_t stream);
 
 /*
  * lb_slice_fold_norm — one rank's row slice of a padded, ragged token batch after a
@@ -207,7 +225,28 @@ lb_status lb_slice_fold_norm(const void *const *partials, int K, int64_t T_pad,
                              const int32_t *set_counts, int num_sets,
                              const void *residual_in, void *residual_out,
                              const float *gamma, void *y_out, uint8_t *q_out,
-                             float *scale_out, int64_t H, float eps, lb_stream_t stream);
+                             float *scale_out, int64_t H, float eps,
+                             const lb_options *options, lb_stream_t stream);
+
+/*
+ * lb_slice_fold_norm_v — one rank's rows of a padded, ragged token batch after a
+ * variable-size attention-DP reduce-scatter ("Layer boundaries", section "Choose a
+ * reduction policy", value rsv; section "Token layouts and sums": ATTN_DP token
+ * sets): rank `set` receives exactly the valid rows of its own token set, global
+ * rows [set_offsets[set], set_offsets[set] + set_counts[set]), no padding.
+ *
+ *   partials       K device pointers, each bf16 [T_pad,H] over the padded batch
+ *   set            0 <= set < num_sets (1 <= num_sets <= LB_MAX_SETS)
+ *   set_offsets, set_counts   host int32 [num_sets], as for lb_slice_fold_norm
+ *   residual_in    bf16 [set_counts[set], H] or NULL (Initial)
+ *   residual_out, y_out, q_out/scale_out: compact [set_counts[set], ...] outputs
+ */
+lb_status lb_slice_fold_norm_v(const void *const *partials, int K, int64_t T_pad, int set,
+                               const int32_t *set_offsets, const int32_t *set_counts,
+                               int num_sets, const void *residual_in, void *residual_out,
+                               const float *gamma, void *y_out, uint8_t *q_out,
+                               float *scale_out, int64_t H, float eps,
+                               const lb_options *options, lb_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -195,6 +195,24 @@ lb_status check_stream_buffers(const void *residual_in, void *residual_out,
     return LB_OK;
 }
 
+// Options: known flags only; the snapshot is one more output of residual's shape.
+lb_status check_options(const lb_options *opt, int64_t rows, int64_t H, BufList *l) {
+    if (opt == nullptr)
+        return LB_OK;
+    if (opt->flags & ~static_cast<unsigned int>(LB_OPT_GEMMA_WEIGHT))
+        return LB_ERR_UNSUPPORTED;
+    if (opt->residual_snapshot != nullptr) {
+        LB_TRY(check_tensor(opt->residual_snapshot));
+        l->add(opt->residual_snapshot, static_cast<uint64_t>(rows * H * 2), true);
+    }
+    return LB_OK;
+}
+
+void set_options(lb::Params *p, const lb_options *opt) {
+    p->gemma = (opt != nullptr && (opt->flags & LB_OPT_GEMMA_WEIGHT)) ? 1 : 0;
+    p->snapshot = opt != nullptr ? static_cast<uint16_t *>(opt->residual_snapshot) : nullptr;
+}
+
 void set_stream_params(lb::Params *p, const void *residual_in, void *residual_out,
                        const float *gamma, void *y_out, uint8_t *q_out, float *scale_out,
                        int64_t rows, int64_t H, float eps) {
@@ -212,7 +230,7 @@ void set_stream_params(lb::Params *p, const void *residual_in, void *residual_ou
 lb_status fold_common(const void *const *partials, int K, const void *residual_in,
                       void *residual_out, const float *gamma, void *y_out, uint8_t *q_out,
                       float *scale_out, int64_t T, int64_t H, float eps,
-                      lb_stream_t stream) {
+                      const lb_options *opt, lb_stream_t stream) {
     LB_TRY(check_shape(T, H, eps));
     if (K < 0)
         return LB_ERR_INVALID_ARGUMENT;
@@ -224,6 +242,7 @@ lb_status fold_common(const void *const *partials, int K, const void *residual_i
     LB_TRY(check_fold_inputs(partials, K, T, residual_in, &l, H));
     LB_TRY(check_stream_buffers(residual_in, residual_out, gamma, y_out, q_out, scale_out, T,
                                 H, &l));
+    LB_TRY(check_options(opt, T, H, &l));
     LB_TRY(check_overlaps(l));
     lb::Params p;
     std::memset(&p, 0, sizeof p);
@@ -232,8 +251,28 @@ lb_status fold_common(const void *const *partials, int K, const void *residual_i
     p.K = K;
     set_stream_params(&p, residual_in, residual_out, gamma, y_out, q_out, scale_out, T, H,
                       eps);
+    set_options(&p, opt);
     return launch(p, lb::kFold, q_out != nullptr, K + (residual_in != nullptr ? 1 : 0),
                   reinterpret_cast<cudaStream_t>(stream));
+}
+
+// Shared validation of the ragged set metadata: sets ascending, disjoint, inside.
+lb_status check_sets(const int32_t *set_offsets, const int32_t *set_counts, int num_sets,
+                     int64_t T_pad) {
+    if (num_sets < 0)
+        return LB_ERR_INVALID_ARGUMENT;
+    if (num_sets > LB_MAX_SETS)
+        return LB_ERR_UNSUPPORTED;
+    if (num_sets > 0 && (set_offsets == nullptr || set_counts == nullptr))
+        return LB_ERR_INVALID_ARGUMENT;
+    int64_t prev_end = 0;
+    for (int s = 0; s < num_sets; ++s) {
+        const int64_t lo = set_offsets[s], n = set_counts[s];
+        if (lo < prev_end || n < 0 || lo + n > T_pad)
+            return LB_ERR_INVALID_ARGUMENT;
+        prev_end = lo + n;
+    }
+    return LB_OK;
 }
 
 }  // namespace
@@ -396,19 +435,19 @@ lb_status lb_device_error(unsigned int *flags, int clear) {
 
 lb_status lb_fold_norm(const void *const *partials, int K, const void *residual_in,
                        void *residual_out, const float *gamma, void *y_out, int64_t T,
-                       int64_t H, float eps, lb_stream_t stream) {
+                       int64_t H, float eps, const lb_options *options, lb_stream_t stream) {
     return fold_common(partials, K, residual_in, residual_out, gamma, y_out, nullptr,
-                       nullptr, T, H, eps, stream);
+                       nullptr, T, H, eps, options, stream);
 }
 
 lb_status lb_fold_norm_fp8(const void *const *partials, int K, const void *residual_in,
                            void *residual_out, const float *gamma, uint8_t *q_out,
                            float *scale_out, void *y_out, int64_t T, int64_t H, float eps,
-                           lb_stream_t stream) {
+                           const lb_options *options, lb_stream_t stream) {
     if (q_out == nullptr || scale_out == nullptr)
         return LB_ERR_INVALID_ARGUMENT;
     return fold_common(partials, K, residual_in, residual_out, gamma, y_out, q_out,
-                       scale_out, T, H, eps, stream);
+                       scale_out, T, H, eps, options, stream);
 }
 
 lb_status lb_moe_finalize_fold_norm(const void *expert_out, int64_t n_expert_rows,
@@ -416,7 +455,8 @@ lb_status lb_moe_finalize_fold_norm(const void *expert_out, int64_t n_expert_row
                                     const void *residual_in, void *residual_out,
                                     const float *gamma, void *y_out, uint8_t *q_out,
                                     float *scale_out, int64_t T, int64_t H, float eps,
-                                    int32_t *bad_index_flag, lb_stream_t stream) {
+                                    int32_t *bad_index_flag, const lb_options *options,
+                                    lb_stream_t stream) {
     LB_TRY(check_shape(T, H, eps));
     if (topk < 1 || n_expert_rows < 0)
         return LB_ERR_INVALID_ARGUMENT;
@@ -437,6 +477,7 @@ lb_status lb_moe_finalize_fold_norm(const void *expert_out, int64_t n_expert_row
     l.add(bad_index_flag, 4, true);
     LB_TRY(check_stream_buffers(residual_in, residual_out, gamma, y_out, q_out, scale_out, T,
                                 H, &l));
+    LB_TRY(check_options(options, T, H, &l));
     LB_TRY(check_overlaps(l));
     lb::Params p;
     std::memset(&p, 0, sizeof p);
@@ -448,6 +489,7 @@ lb_status lb_moe_finalize_fold_norm(const void *expert_out, int64_t n_expert_row
     p.bad_index = bad_index_flag;
     set_stream_params(&p, residual_in, residual_out, gamma, y_out, q_out, scale_out, T, H,
                       eps);
+    set_options(&p, options);
     return launch(p, lb::kMoe, q_out != nullptr, topk + (residual_in != nullptr ? 1 : 0),
                   reinterpret_cast<cudaStream_t>(stream));
 }
@@ -457,21 +499,14 @@ lb_status lb_slice_fold_norm(const void *const *partials, int K, int64_t T_pad,
                              const int32_t *set_counts, int num_sets,
                              const void *residual_in, void *residual_out,
                              const float *gamma, void *y_out, uint8_t *q_out,
-                             float *scale_out, int64_t H, float eps, lb_stream_t stream) {
+                             float *scale_out, int64_t H, float eps,
+                             const lb_options *options, lb_stream_t stream) {
     if (T_pad < 0 || num_slices < 1 || T_pad % num_slices != 0 || slice < 0 ||
         slice >= num_slices || num_sets < 0)
         return LB_ERR_INVALID_ARGUMENT;
     if (num_sets > LB_MAX_SETS || T_pad > INT32_MAX)
         return LB_ERR_UNSUPPORTED;
-    if (num_sets > 0 && (set_offsets == nullptr || set_counts == nullptr))
-        return LB_ERR_INVALID_ARGUMENT;
-    int64_t prev_end = 0;
-    for (int s = 0; s < num_sets; ++s) {
-        const int64_t lo = set_offsets[s], n = set_counts[s];
-        if (lo < prev_end || n < 0 || lo + n > T_pad)
-            return LB_ERR_INVALID_ARGUMENT;  // sets must be ascending, disjoint, inside
-        prev_end = lo + n;
-    }
+    LB_TRY(check_sets(set_offsets, set_counts, num_sets, T_pad));
     const int64_t S = T_pad / num_slices;
     LB_TRY(check_shape(S, H, eps));
     if (K < 0)
@@ -484,6 +519,7 @@ lb_status lb_slice_fold_norm(const void *const *partials, int K, int64_t T_pad,
     LB_TRY(check_fold_inputs(partials, K, T_pad, residual_in, &l, H));
     LB_TRY(check_stream_buffers(residual_in, residual_out, gamma, y_out, q_out, scale_out, S,
                                 H, &l));
+    LB_TRY(check_options(options, S, H, &l));
     LB_TRY(check_overlaps(l));
     lb::Params p;
     std::memset(&p, 0, sizeof p);
@@ -503,6 +539,45 @@ lb_status lb_slice_fold_norm(const void *const *partials, int K, int64_t T_pad,
         return LB_OK;                          // the slice holds padding only
     set_stream_params(&p, residual_in, residual_out, gamma, y_out, q_out, scale_out, S, H,
                       eps);
+    set_options(&p, options);
+    return launch(p, lb::kFold, q_out != nullptr, K + (residual_in != nullptr ? 1 : 0),
+                  reinterpret_cast<cudaStream_t>(stream));
+}
+
+lb_status lb_slice_fold_norm_v(const void *const *partials, int K, int64_t T_pad, int set,
+                               const int32_t *set_offsets, const int32_t *set_counts,
+                               int num_sets, const void *residual_in, void *residual_out,
+                               const float *gamma, void *y_out, uint8_t *q_out,
+                               float *scale_out, int64_t H, float eps,
+                               const lb_options *options, lb_stream_t stream) {
+    if (T_pad < 0 || num_sets < 1 || set < 0 || set >= num_sets)
+        return LB_ERR_INVALID_ARGUMENT;
+    if (num_sets > LB_MAX_SETS || T_pad > INT32_MAX)
+        return LB_ERR_UNSUPPORTED;
+    LB_TRY(check_sets(set_offsets, set_counts, num_sets, T_pad));
+    const int64_t rows = set_counts[set];
+    LB_TRY(check_shape(rows, H, eps));
+    if (K < 0)
+        return LB_ERR_INVALID_ARGUMENT;
+    if (K > LB_MAX_K)
+        return LB_ERR_UNSUPPORTED;
+    if (rows == 0)
+        return LB_OK;                          // empty set: no pointer is used
+    BufList l;
+    LB_TRY(check_fold_inputs(partials, K, T_pad, residual_in, &l, H));
+    LB_TRY(check_stream_buffers(residual_in, residual_out, gamma, y_out, q_out, scale_out,
+                                rows, H, &l));
+    LB_TRY(check_options(options, rows, H, &l));
+    LB_TRY(check_overlaps(l));
+    lb::Params p;
+    std::memset(&p, 0, sizeof p);
+    for (int k = 0; k < K; ++k)
+        p.partials[k] = static_cast<const uint16_t *>(partials[k]);
+    p.K = K;
+    p.in_row0 = set_offsets[set];              // every row of the set is valid
+    set_stream_params(&p, residual_in, residual_out, gamma, y_out, q_out, scale_out, rows, H,
+                      eps);
+    set_options(&p, options);
     return launch(p, lb::kFold, q_out != nullptr, K + (residual_in != nullptr ? 1 : 0),
                   reinterpret_cast<cudaStream_t>(stream));
 }

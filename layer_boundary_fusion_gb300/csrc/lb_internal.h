@@ -53,6 +53,8 @@ struct Params {
     const uint16_t *residual_in;
     uint16_t *residual_out;
     const float *gamma;
+    int gemma;                 // read weight = 1 + gamma
+    uint16_t *snapshot;        // optional second copy of residual'
     uint16_t *y_out;
     uint8_t *q_out;
     float *scale_out;

@@ -215,6 +215,11 @@ __global__ void __launch_bounds__(512, 1) boundary_kernel(const __grid_constant_
             gm[i][1] = make_float2(a.z, a.w);
             gm[i][2] = make_float2(b.x, b.y);
             gm[i][3] = make_float2(b.z, b.w);
+            if (p.gemma) {                         // GemmaRMSNorm: weight = 1 + gamma
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    gm[i][e] = __fadd2_rn(make_float2(1.0f, 1.0f), gm[i][e]);
+            }
         } else {
 #pragma unroll
             for (int e = 0; e < 4; ++e)
@@ -313,11 +318,16 @@ __global__ void __launch_bounds__(512, 1) boundary_kernel(const __grid_constant_
                     acc[i][e] = __fadd2_rn(acc[i][e], f[e]);
             }
     }
-    if (p.residual_out != nullptr) {
+    if (p.residual_out != nullptr || p.snapshot != nullptr) {
 #pragma unroll
         for (int i = 0; i < kVpt; ++i)
-            if (act[i])
-                *reinterpret_cast<uint4 *>(p.residual_out + row * H + col[i]) = pack8x2(acc[i]);
+            if (act[i]) {
+                const uint4 packed = pack8x2(acc[i]);
+                if (p.residual_out != nullptr)
+                    *reinterpret_cast<uint4 *>(p.residual_out + row * H + col[i]) = packed;
+                if (p.snapshot != nullptr)
+                    *reinterpret_cast<uint4 *>(p.snapshot + row * H + col[i]) = packed;
+            }
     }
     if (!need_read)
         return;                                    // complete_output / fold only

@@ -367,6 +367,11 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
             gm[i][1] = make_float2(a.z, a.w);
             gm[i][2] = make_float2(b.x, b.y);
             gm[i][3] = make_float2(b.z, b.w);
+            if (p.gemma) {                         // GemmaRMSNorm: weight = 1 + gamma
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    gm[i][e] = __fadd2_rn(make_float2(1.0f, 1.0f), gm[i][e]);
+            }
         } else {
 #pragma unroll
             for (int e = 0; e < 4; ++e)
@@ -442,12 +447,16 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
         if (ok && lane == 0)
             mbar_arrive(empty0 + 8 * s);
         const int64_t roff = row * p.H;
-        if (ok && p.residual_out != nullptr) {
+        if (ok && (p.residual_out != nullptr || p.snapshot != nullptr)) {
 #pragma unroll
             for (int v = 0; v < kVpt; ++v)
-                if (act[v])
-                    *reinterpret_cast<uint4 *>(p.residual_out + roff + col[v]) =
-                        pack8x2(acc[v]);
+                if (act[v]) {
+                    const uint4 packed = pack8x2(acc[v]);
+                    if (p.residual_out != nullptr)
+                        *reinterpret_cast<uint4 *>(p.residual_out + roff + col[v]) = packed;
+                    if (p.snapshot != nullptr)
+                        *reinterpret_cast<uint4 *>(p.snapshot + roff + col[v]) = packed;
+                }
         }
         if (!need_read) {
             if (!ok) {

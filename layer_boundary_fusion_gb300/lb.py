@@ -30,10 +30,11 @@ LB_KERNEL_ROW = 0
 LB_KERNEL_STREAM = 1
 LB_DEVICE_ERR_TIMEOUT = 1
 LB_DEVICE_ERR_LAUNCH = 2
+LB_OPT_GEMMA_WEIGHT = 1
 
 EXPORTED = ("lb_status_string", "lb_last_cuda_error", "lb_version", "lb_launch_plan",
             "lb_device_error", "lb_fold_norm", "lb_fold_norm_fp8",
-            "lb_moe_finalize_fold_norm", "lb_slice_fold_norm")
+            "lb_moe_finalize_fold_norm", "lb_slice_fold_norm", "lb_slice_fold_norm_v")
 
 
 class Plan(ctypes.Structure):
@@ -45,6 +46,11 @@ class Plan(ctypes.Structure):
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+class Options(ctypes.Structure):
+    """lb_options: optional behaviour of a call."""
+    _fields_ = [("flags", ctypes.c_uint), ("residual_snapshot", ctypes.c_void_p)]
 
 
 class LibraryMissing(RuntimeError):
@@ -89,18 +95,23 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.lb_launch_plan.restype = _int
     lib.lb_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), _int]
     lib.lb_device_error.restype = _int
+    op = ctypes.POINTER(Options)
     lib.lb_fold_norm.argtypes = [ctypes.POINTER(_vp), _int, _vp, _vp, _vp, _vp, _i64, _i64,
-                                 _f32, _vp]
+                                 _f32, op, _vp]
     lib.lb_fold_norm.restype = _int
     lib.lb_fold_norm_fp8.argtypes = [ctypes.POINTER(_vp), _int, _vp, _vp, _vp, _vp, _vp, _vp,
-                                     _i64, _i64, _f32, _vp]
+                                     _i64, _i64, _f32, op, _vp]
     lib.lb_fold_norm_fp8.restype = _int
     lib.lb_moe_finalize_fold_norm.argtypes = [_vp, _i64, _vp, _vp, _int, _vp, _vp, _vp, _vp,
-                                              _vp, _vp, _i64, _i64, _f32, _vp, _vp]
+                                              _vp, _vp, _i64, _i64, _f32, _vp, op, _vp]
     lib.lb_moe_finalize_fold_norm.restype = _int
     lib.lb_slice_fold_norm.argtypes = [ctypes.POINTER(_vp), _int, _i64, _int, _int, _vp, _vp,
-                                       _int, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _f32, _vp]
+                                       _int, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _f32, op, _vp]
     lib.lb_slice_fold_norm.restype = _int
+    lib.lb_slice_fold_norm_v.argtypes = [ctypes.POINTER(_vp), _int, _i64, _int, _vp, _vp,
+                                         _int, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _f32, op,
+                                         _vp]
+    lib.lb_slice_fold_norm_v.restype = _int
     _lib = lib
     return lib
 
@@ -130,6 +141,13 @@ def _ptr_array(items: Sequence) -> ctypes.Array:
     for i, x in enumerate(items):
         arr[i] = _ptr(x)
     return arr
+
+
+def _options(gemma: bool, residual_snapshot):
+    """lb_options for the keyword arguments, or None (NULL) for the defaults."""
+    if not gemma and residual_snapshot is None:
+        return None
+    return ctypes.byref(Options(LB_OPT_GEMMA_WEIGHT if gemma else 0, _ptr(residual_snapshot)))
 
 
 def _check(status: int, func: str) -> None:
@@ -162,52 +180,78 @@ def lb_device_error(clear: bool = True) -> int:
 
 
 def lb_fold_norm(partials, residual_in, residual_out, gamma, y_out, T, H, eps,
-                 stream=None) -> None:
+                 stream=None, *, gemma=False, residual_snapshot=None) -> None:
     lib = load()
     partials = list(partials)
     s = _stream(stream, *partials, residual_in, residual_out, y_out)
     _check(lib.lb_fold_norm(_ptr_array(partials), len(partials), _ptr(residual_in),
-                            _ptr(residual_out), _ptr(gamma), _ptr(y_out), T, H, eps, s),
+                            _ptr(residual_out), _ptr(gamma), _ptr(y_out), T, H, eps,
+                            _options(gemma, residual_snapshot), s),
            "lb_fold_norm")
 
 
 def lb_fold_norm_fp8(partials, residual_in, residual_out, gamma, q_out, scale_out, y_out,
-                     T, H, eps, stream=None) -> None:
+                     T, H, eps, stream=None, *, gemma=False, residual_snapshot=None) -> None:
     lib = load()
     partials = list(partials)
     s = _stream(stream, *partials, residual_in, residual_out, q_out)
     _check(lib.lb_fold_norm_fp8(_ptr_array(partials), len(partials), _ptr(residual_in),
                                 _ptr(residual_out), _ptr(gamma), _ptr(q_out),
-                                _ptr(scale_out), _ptr(y_out), T, H, eps, s),
+                                _ptr(scale_out), _ptr(y_out), T, H, eps,
+                                _options(gemma, residual_snapshot), s),
            "lb_fold_norm_fp8")
 
 
 def lb_moe_finalize_fold_norm(expert_out, n_expert_rows, idx, w, topk, residual_in,
                               residual_out, gamma, y_out, q_out, scale_out, T, H, eps,
-                              bad_index_flag=None, stream=None) -> None:
+                              bad_index_flag=None, stream=None, *, gemma=False,
+                              residual_snapshot=None) -> None:
     lib = load()
     s = _stream(stream, expert_out, residual_out, y_out, q_out)
     _check(lib.lb_moe_finalize_fold_norm(_ptr(expert_out), n_expert_rows, _ptr(idx), _ptr(w),
                                          topk, _ptr(residual_in), _ptr(residual_out),
                                          _ptr(gamma), _ptr(y_out), _ptr(q_out),
                                          _ptr(scale_out), T, H, eps, _ptr(bad_index_flag),
-                                         s),
+                                         _options(gemma, residual_snapshot), s),
            "lb_moe_finalize_fold_norm")
+
+
+def _int32_array(values):
+    n = len(values)
+    return (ctypes.c_int32 * max(1, n))(*[int(v) for v in values]), n
 
 
 def lb_slice_fold_norm(partials, T_pad, num_slices, slice_, set_offsets, set_counts,
                        residual_in, residual_out, gamma, y_out, q_out, scale_out, H, eps,
-                       stream=None) -> None:
+                       stream=None, *, gemma=False, residual_snapshot=None) -> None:
     lib = load()
     partials = list(partials)
-    n = len(set_offsets)
-    if len(set_counts) != n:
+    if len(set_offsets) != len(set_counts):
         raise ValueError("set_offsets and set_counts differ in length")
-    offs = (ctypes.c_int32 * max(1, n))(*[int(v) for v in set_offsets])
-    cnts = (ctypes.c_int32 * max(1, n))(*[int(v) for v in set_counts])
+    offs, n = _int32_array(set_offsets)
+    cnts, _ = _int32_array(set_counts)
     s = _stream(stream, *partials, residual_out, y_out, q_out)
     _check(lib.lb_slice_fold_norm(_ptr_array(partials), len(partials), T_pad, num_slices,
                                   slice_, ctypes.cast(offs, _vp), ctypes.cast(cnts, _vp), n,
                                   _ptr(residual_in), _ptr(residual_out), _ptr(gamma),
-                                  _ptr(y_out), _ptr(q_out), _ptr(scale_out), H, eps, s),
+                                  _ptr(y_out), _ptr(q_out), _ptr(scale_out), H, eps,
+                                  _options(gemma, residual_snapshot), s),
            "lb_slice_fold_norm")
+
+
+def lb_slice_fold_norm_v(partials, T_pad, set_, set_offsets, set_counts, residual_in,
+                         residual_out, gamma, y_out, q_out, scale_out, H, eps, stream=None, *,
+                         gemma=False, residual_snapshot=None) -> None:
+    lib = load()
+    partials = list(partials)
+    if len(set_offsets) != len(set_counts):
+        raise ValueError("set_offsets and set_counts differ in length")
+    offs, n = _int32_array(set_offsets)
+    cnts, _ = _int32_array(set_counts)
+    s = _stream(stream, *partials, residual_out, y_out, q_out)
+    _check(lib.lb_slice_fold_norm_v(_ptr_array(partials), len(partials), T_pad, set_,
+                                    ctypes.cast(offs, _vp), ctypes.cast(cnts, _vp), n,
+                                    _ptr(residual_in), _ptr(residual_out), _ptr(gamma),
+                                    _ptr(y_out), _ptr(q_out), _ptr(scale_out), H, eps,
+                                    _options(gemma, residual_snapshot), s),
+           "lb_slice_fold_norm_v")

@@ -33,7 +33,7 @@ def declared_functions():
 def test_header_declares_the_four_boundary_calls():
     names = declared_functions()
     for f in ("lb_fold_norm", "lb_fold_norm_fp8", "lb_moe_finalize_fold_norm",
-              "lb_slice_fold_norm"):
+              "lb_slice_fold_norm", "lb_slice_fold_norm_v"):
         assert f in names
 
 
@@ -138,7 +138,12 @@ def run(name, fn, *args):
         results[name] = e.status
 f = lb.lb_fold_norm
 run("ok_empty", f, P, a(2), a(3), a(4), a(5), 0, H, 1e-6, 0)
-results["K_negative"] = L.lb_fold_norm(None, -1, a(2), a(3), a(4), a(5), T, H, 1e-6, None)
+results["K_negative"] = L.lb_fold_norm(None, -1, a(2), a(3), a(4), a(5), T, H, 1e-6, None, None)
+opts = lb.Options(7, None)
+results["unknown_flag"] = L.lb_fold_norm((lb._vp * 2)(a(0), a(1)), 2, a(2), a(3), a(4), a(5), T, H, 1e-6, lb.ctypes.byref(opts), None)
+run("snapshot_misaligned", lambda: f(P, a(2), a(3), a(4), a(5), T, H, 1e-6, 0, residual_snapshot=a(9) + 8))
+run("snapshot_overlaps_y", lambda: f(P, a(2), a(3), a(4), a(5), T, H, 1e-6, 0, residual_snapshot=a(5) + 16))
+run("snapshot_empty_ok", lambda: f(P, a(2), a(3), a(4), a(5), 0, H, 1e-6, 0, gemma=True, residual_snapshot=a(9)))
 run("K_too_big", f, [a(i) for i in range(17)], a(20), a(21), a(22), a(23), T, H, 1e-6, 0)
 run("partial_null", f, [a(0), None], a(2), a(3), a(4), a(5), T, H, 1e-6, 0)
 run("partial_misaligned", f, [a(0), a(1) + 8], a(2), a(3), a(4), a(5), T, H, 1e-6, 0)
@@ -191,6 +196,14 @@ run("slice_set_past_end", s, P, 2032, 8, 3, [0, 40, 552, 570], cnt, a(2), a(3), 
 run("slice_count_negative", s, P, 2032, 8, 3, off, [37, -1, 5, 1470], a(2), a(3), a(4), a(5), None, None, H, 1e-6, 0)
 run("slice_too_many_sets", s, P, 2032, 8, 3, list(range(65)), [0] * 65, a(2), a(3), a(4), a(5), None, None, H, 1e-6, 0)
 run("slice_padding_only_ok", s, P, 2032, 8, 7, [0], [8], a(2), a(3), a(4), a(5), None, None, H, 1e-6, 0)
+v = lb.lb_slice_fold_norm_v
+run("rsv_empty_set_ok", v, P, 2032, 1, [0, 40], [37, 0], a(2), a(3), a(4), a(5), None, None, H, 1e-6, 0)
+run("rsv_set_high", v, P, 2032, 4, off, cnt, a(2), a(3), a(4), a(5), None, None, H, 1e-6, 0)
+run("rsv_set_negative", v, P, 2032, -1, off, cnt, a(2), a(3), a(4), a(5), None, None, H, 1e-6, 0)
+run("rsv_no_sets", v, P, 2032, 0, [], [], a(2), a(3), a(4), a(5), None, None, H, 1e-6, 0)
+run("rsv_sets_overlap", v, P, 2032, 1, [0, 30, 552, 560], cnt, a(2), a(3), a(4), a(5), None, None, H, 1e-6, 0)
+run("rsv_set_past_end", v, P, 2000, 3, off, cnt, a(2), a(3), a(4), a(5), None, None, H, 1e-6, 0)
+run("rsv_nothing_to_write", v, P, 2032, 3, off, cnt, a(2), None, a(4), None, None, None, H, 1e-6, 0)
 print(json.dumps(results))
 """
 
@@ -211,6 +224,10 @@ EXPECTED = {
     "slice_index_negative": 1, "slice_zero_slices": 1, "slice_sets_overlap": 1,
     "slice_sets_descending": 1, "slice_set_past_end": 1, "slice_count_negative": 1,
     "slice_too_many_sets": 3, "slice_padding_only_ok": 0,
+    "unknown_flag": 3, "snapshot_misaligned": 2, "snapshot_overlaps_y": 1,
+    "snapshot_empty_ok": 0,
+    "rsv_empty_set_ok": 0, "rsv_set_high": 1, "rsv_set_negative": 1, "rsv_no_sets": 1,
+    "rsv_sets_overlap": 1, "rsv_set_past_end": 1, "rsv_nothing_to_write": 1,
 }
 
 

@@ -436,3 +436,116 @@ def test_runs_on_a_side_stream(lb):
     s.synchronize()
     assert_bits_equal(host_bits(ro), want["residual_out"], "side stream residual'")
     assert_bf16_close(host_bits(yo), want["y"], "side stream y")
+
+
+# --------------------------------------------------------------------------------------
+# Gemma weight (1 + gamma), residual snapshot, variable-size reduce-scatter (rsv)
+# --------------------------------------------------------------------------------------
+
+def _options_fold(lb, w, *, fp8, gemma, snapshot):
+    T, H = w.T, w.H
+    P = [dev_bits(p) for p in w.partials]
+    R = dev_bits(w.residual)
+    G = torch.from_numpy(w.gamma).cuda()
+    ro, yo = Guarded(T, H, torch.bfloat16), Guarded(T, H, torch.bfloat16)
+    sn = Guarded(T, H, torch.bfloat16) if snapshot else None
+    qo = Guarded(T, H, torch.uint8) if fp8 else None
+    so = Guarded(T, 0, torch.float32) if fp8 else None
+    kw = dict(gemma=gemma, residual_snapshot=sn.t if sn else None)
+    if fp8:
+        lb.lb_fold_norm_fp8(P, R, ro.t, G, qo.t, so.t, yo.t, T, H, w.eps, **kw)
+    else:
+        lb.lb_fold_norm(P, R, ro.t, G, yo.t, T, H, w.eps, **kw)
+    torch.cuda.synchronize()
+    out = {"residual_out": ro, "y": yo}
+    if snapshot:
+        out["snapshot"] = sn
+    if fp8:
+        out.update(q=qo, scale=so)
+    for g in out.values():
+        g.check()
+    return {k: g.host() for k, g in out.items()}
+
+
+@pytest.mark.parametrize("T", [50, 700])
+@pytest.mark.parametrize("fp8", [False, True])
+def test_gemma_weight_and_snapshot(lb, T, fp8):
+    w = wl.fold_workload("gem", 3, T, 2048, seed=93 + T)
+    w.gamma = (0.05 * np.random.default_rng(T).standard_normal(w.H)).astype(np.float32)
+    want = oracle.fold_norm(w.partials, w.residual, w.gamma, w.eps, want_fp8=True, gemma=True)
+    got = _options_fold(lb, w, fp8=fp8, gemma=True, snapshot=True)
+    check_fold(got, want, f"gemma T={T}")
+    assert_bits_equal(got["snapshot"], want["residual_out"], "snapshot")
+    plain = oracle.fold_norm(w.partials, w.residual, w.gamma, w.eps)
+    assert not np.array_equal(plain["y"], want["y"])
+
+
+def test_moe_terminal_handoff_with_gemma_norm(lb):
+    """The terminal layer's deferred MoE finalize fused with the final (Gemma) norm."""
+    w = wl.moe_workload("term", 300, 2048, 32, 8, seed=94)
+    w.gamma = (0.05 * np.random.default_rng(9).standard_normal(w.H)).astype(np.float32)
+    want = oracle.moe_finalize_fold_norm(w.expert_out, w.idx, w.w, w.residual, w.gamma, w.eps,
+                                         gemma=True)
+    E, I = dev_bits(w.expert_out), torch.from_numpy(w.idx).cuda()
+    Wt, R = torch.from_numpy(w.w).cuda(), dev_bits(w.residual)
+    G = torch.from_numpy(w.gamma).cuda()
+    ro, yo, sn = (Guarded(w.T, w.H, torch.bfloat16) for _ in range(3))
+    lb.lb_moe_finalize_fold_norm(E, w.expert_out.shape[0], I, Wt, w.topk, R, ro.t, G, yo.t,
+                                 None, None, w.T, w.H, w.eps, gemma=True,
+                                 residual_snapshot=sn.t)
+    torch.cuda.synchronize()
+    for g in (ro, yo, sn):
+        g.check()
+    got = {"residual_out": ro.host(), "y": yo.host()}
+    check_fold(got, want, "moe + gemma norm")
+    assert_bits_equal(sn.host(), want["residual_out"], "moe snapshot")
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_rsv_every_rank(lb, fp8):
+    w = wl.ragged_slice()
+    P = [dev_bits(p) for p in w.partials]
+    G = torch.from_numpy(w.gamma).cuda()
+    for s, (o, c) in enumerate(zip(w.set_offsets.tolist(), w.set_counts.tolist())):
+        res = w.residual_full[o:o + c]
+        want = oracle.set_slice_fold_norm(w.partials, w.T_pad, s, w.set_offsets,
+                                          w.set_counts, res, w.gamma, w.eps, want_fp8=fp8,
+                                          gemma=(s % 2 == 1))
+        R = dev_bits(res)
+        ro, yo = Guarded(c, w.H, torch.bfloat16), Guarded(c, w.H, torch.bfloat16)
+        qo = Guarded(c, w.H, torch.uint8) if fp8 else None
+        so = Guarded(c, 0, torch.float32) if fp8 else None
+        before = _snapshot(P + [R, G])
+        lb.lb_slice_fold_norm_v(P, w.T_pad, s, w.set_offsets, w.set_counts, R, ro.t, G, yo.t,
+                                qo.t if fp8 else None, so.t if fp8 else None, w.H, w.eps,
+                                gemma=(s % 2 == 1))
+        torch.cuda.synchronize()
+        _assert_unchanged(before, P + [R, G])
+        outs = {"residual_out": ro, "y": yo}
+        if fp8:
+            outs.update(q=qo, scale=so)
+        for g in outs.values():
+            g.check()
+        check_fold({k: g.host() for k, g in outs.items()}, want, f"rsv rank {s}")
+
+
+def test_slice_with_gemma_and_snapshot(lb):
+    w = wl.ragged_slice(slice_=2)
+    S = w.T
+    want = oracle.slice_fold_norm(w.partials, w.T_pad, 8, 2, w.set_offsets, w.set_counts,
+                                  w.residual_full[2 * S:3 * S], w.gamma, w.eps, gemma=True,
+                                  out={"residual_out": np.full((S, w.H), SENTINEL16, np.uint16),
+                                       "y": np.full((S, w.H), SENTINEL16, np.uint16)})
+    P = [dev_bits(p) for p in w.partials]
+    R = dev_bits(w.residual_full[2 * S:3 * S])
+    G = torch.from_numpy(w.gamma).cuda()
+    ro, yo, sn = (Guarded(S, w.H, torch.bfloat16) for _ in range(3))
+    lb.lb_slice_fold_norm(P, w.T_pad, 8, 2, w.set_offsets, w.set_counts, R, ro.t, G, yo.t,
+                          None, None, w.H, w.eps, gemma=True, residual_snapshot=sn.t)
+    torch.cuda.synchronize()
+    for g in (ro, yo, sn):
+        g.check()
+    assert_bits_equal(ro.host(), want["residual_out"], "slice residual' (incl. padding)")
+    assert_bits_equal(sn.host(), want["residual_out"], "slice snapshot (incl. padding)")
+    valid = ~np.all(want["y"] == SENTINEL16, axis=1)
+    assert_bf16_close(yo.host(), want["y"], "slice gemma y", rows=valid)
