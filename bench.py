@@ -340,6 +340,22 @@ def measure_variants(lb, dev, stream, dist, steps):
     record("ragged_slice", v, nb, el, steps, plan_of(lb, S, w.H, w.K + 1, props),
            f"rotated {ns} sets")
     del sets, ls, P0
+    # variable-size reduce-scatter (rsv): ranks 1 (512 rows) and 3 (1470 rows)
+    for rank in (1, 3):
+        o, c = int(w.set_offsets[rank]), int(w.set_counts[rank])
+        nb = bytes_fold(w.K, c, w.H)
+        ns = n_sets(nb, dev)
+        P0 = [dev_bits(p, dev) for p in w.partials]
+        R0 = dev_bits(w.residual_full[o:o + c], dev)
+        sets = [([p.clone() for p in P0], R0.clone(), torch.empty_like(R0),
+                 torch.empty_like(R0)) for _ in range(ns)]
+        ls = [(lambda s=s, rank=rank: lb.lb_slice_fold_norm_v(
+            s[0], w.T_pad, rank, w.set_offsets, w.set_counts, s[1], s[2], G, s[3], None, None,
+            w.H, w.eps, stream=sp)) for s in sets]
+        el, _ = time_graph(ls, steps, 20, stream, dist)
+        record(f"ragged_rsv_rank{rank}", c, nb, el, steps, plan_of(lb, c, w.H, w.K + 1, props),
+               f"rotated {ns} sets")
+        del sets, ls, P0
     # MoE finalize T=1024 top-8
     w = wl.moe_finalize()
     nb = bytes_moe(w.T, w.H, w.topk)
@@ -421,7 +437,9 @@ def run_native(args, dist):
     peak, peak_src = peak_hbm()
     achieved = nbytes / per_launch / 1e9
 
-    # end to end through the public API: pinned host inputs -> device -> call -> host
+    # end to end through the public API: pinned host inputs -> device -> call -> host,
+    # each step copying its inputs in and its results out, overlapped in row chunks
+    from layer_boundary_fusion_gb300.host import HostPipeline
     e2e_steps = args.e2e_steps
     hP = [torch.from_numpy(p.view(np.int16)).pin_memory() for p in w.partials]
     hR = torch.from_numpy(w.residual.view(np.int16)).pin_memory()
@@ -429,35 +447,24 @@ def run_native(args, dist):
     hro = torch.empty((w.T, w.H), dtype=torch.int16).pin_memory()
     hq = torch.empty((w.T, w.H), dtype=torch.uint8).pin_memory()
     hs = torch.empty((w.T,), dtype=torch.float32).pin_memory()
-    s0 = sets[0]
     h2d = sum(p.numel() * 2 for p in hP) + hR.numel() * 2 + hG.numel() * 4
     d2h = hro.numel() * 2 + hq.numel() + hs.numel() * 4
-
-    def e2e_step():
-        for d, h in zip(s0.P, hP):
-            d.view(torch.int16).copy_(h, non_blocking=True)
-        s0.R.view(torch.int16).copy_(hR, non_blocking=True)
-        s0.G.copy_(hG, non_blocking=True)
-        lb.lb_fold_norm_fp8(s0.P, s0.R, s0.ro, s0.G, s0.qo, s0.so, None, w.T, w.H, w.eps,
-                            stream=stream.cuda_stream)
-        hro.copy_(s0.ro.view(torch.int16), non_blocking=True)
-        hq.copy_(s0.qo, non_blocking=True)
-        hs.copy_(s0.so, non_blocking=True)
-
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            e2e_step()
+    del sets, launches
+    torch.cuda.empty_cache()
+    pipe = HostPipeline(w.K, w.T, w.H, dev, chunks=4)
+    cur = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        pipe(hP, hR, hG, hro, hq, hs, w.eps, stream=cur)
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     dist.barrier()
-    ev0.record(stream)
-    with torch.cuda.stream(stream):
-        for _ in range(e2e_steps):
-            e2e_step()
-    ev1.record(stream)
+    ev0.record(cur)
+    for _ in range(e2e_steps):
+        pipe(hP, hR, hG, hro, hq, hs, w.eps, stream=cur)
+    ev1.record(cur)
     torch.cuda.synchronize()
     e2e_value, _ = aggregate(ev0.elapsed_time(ev1) / 1e3, w.T, e2e_steps, dist)
-    del sets, launches
+    del pipe
     torch.cuda.empty_cache()
 
     variants = measure_variants(lb, dev, stream, dist, args.variant_steps)
@@ -487,7 +494,11 @@ def run_native(args, dist):
                      "kernel": kernel_name(plan_of(lb, w.T, w.H, w.K + 1, props), "fold", True)},
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": e2e_steps},
+                "steps": e2e_steps,
+                "how": "pinned host buffers; per step gamma and inputs copied in and "
+                       "residual', codes and scales copied out, 4 row chunks overlapping "
+                       "copy-in, kernel and copy-out, one CUDA graph per step "
+                       "(layer_boundary_fusion_gb300.host)"},
         "gpu_launches": args.steps,
         "clocks": clocks,
         "cpu_baseline": cpu,

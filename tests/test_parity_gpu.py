@@ -549,3 +549,25 @@ def test_slice_with_gemma_and_snapshot(lb):
     assert_bits_equal(sn.host(), want["residual_out"], "slice snapshot (incl. padding)")
     valid = ~np.all(want["y"] == SENTINEL16, axis=1)
     assert_bf16_close(yo.host(), want["y"], "slice gemma y", rows=valid)
+
+
+def test_host_pipeline_matches_the_oracle(lb):
+    """Pinned host buffers in, pinned host buffers out, chunks overlapped across three
+    streams and two device buffer sets; three calls in a row."""
+    from layer_boundary_fusion_gb300.host import HostPipeline
+    w = wl.fold_workload("host", 3, 512, 2048, seed=95, fp8=True)
+    want = oracle.fold_norm(w.partials, w.residual, w.gamma, w.eps, want_y=False,
+                            want_fp8=True)
+    pipe = HostPipeline(w.K, w.T, w.H, "cuda:0", chunks=4)
+    hP = [torch.from_numpy(p.view(np.int16)).pin_memory() for p in w.partials]
+    hR = torch.from_numpy(w.residual.view(np.int16)).pin_memory()
+    hG = torch.from_numpy(w.gamma).pin_memory()
+    ro = torch.empty((w.T, w.H), dtype=torch.int16).pin_memory()
+    q = torch.empty((w.T, w.H), dtype=torch.uint8).pin_memory()
+    sc = torch.empty((w.T,), dtype=torch.float32).pin_memory()
+    for call in range(3):                  # the first call captures, the others replay
+        ro.fill_(-1), q.fill_(0x7F), sc.fill_(float("nan"))
+        pipe(hP, hR, hG, ro, q, sc, w.eps)
+        torch.cuda.synchronize()
+        assert_bits_equal(ro.numpy().view(np.uint16), want["residual_out"], f"host residual' {call}")
+        assert_fp8_close(q.numpy(), want["q"], sc.numpy(), want["scale"], f"host fp8 {call}")
