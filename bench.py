@@ -17,11 +17,14 @@ Printed: one JSON line (rank 0).  `--impl reference` times the CPU oracle instea
 on a bounded sample of rows per step.
 """
 import argparse
+import concurrent.futures
 import glob
 import hashlib
 import json
 import math
 import os
+import platform
+import re
 import statistics
 import subprocess
 import sys
@@ -373,6 +376,34 @@ def measure_variants(lb, dev, stream, dist, steps):
     record("moe_finalize", w.T, nb, el, steps, plan_of(lb, w.T, w.H, w.topk + 1, props),
            f"rotated {ns} sets")
     del sets, ls
+    # fusion gain: the same fold + bf16 read as one fused call and as the unfused
+    # fallback of two calls (the completed sum written to a bf16 buffer, then residual
+    # add + RMSNorm of that buffer), both on this library's kernels
+    for name, w in (("prefill_bf16", wl.prefill_fold_norm_fp8()),
+                    ("decode", wl.decode_fold_norm())):
+        nb = bytes_fold(w.K, w.T, w.H)
+        moved = nb + 2 * 2 * w.T * w.H                 # + the sum written and read back
+        ns = n_sets(moved, dev)
+        sets = fold_sets(w, dev, ns, False)
+        fused = [fold_launcher(lb, s, w.T, w.H, w.eps, False, stream) for s in sets]
+        el, _ = time_graph(fused, steps, 20, stream, dist)
+        record(f"{name}_fused", w.T, nb, el, steps,
+               plan_of(lb, w.T, w.H, w.K + 1, props), f"rotated {ns} sets")
+        for s in sets:
+            s.sum = torch.empty_like(s.ro)
+
+        def unfused(s=None, w=w):
+            lb.lb_fold_norm(s.P, None, s.sum, None, None, w.T, w.H, w.eps, stream=sp)
+            lb.lb_fold_norm([s.sum], s.R, s.ro, s.G, s.yo, w.T, w.H, w.eps, stream=sp)
+        ls = [(lambda s=s: unfused(s)) for s in sets]
+        el, _ = time_graph(ls, steps, 20, stream, dist)
+        record(f"{name}_unfused", w.T, nb, el, steps,
+               [plan_of(lb, w.T, w.H, w.K, props), plan_of(lb, w.T, w.H, 2, props)],
+               f"rotated {ns} sets")
+        out[f"{name}_unfused"]["bytes_moved_per_call"] = moved
+        out[f"{name}_fusion_speedup"] = round(out[f"{name}_unfused"]["us_per_call"]
+                                              / out[f"{name}_fused"]["us_per_call"], 3)
+        del sets, ls, fused
     # tiny correctness configuration
     w = wl.tiny_fold_norm()
     nb = bytes_fold(w.K, w.T, w.H)
@@ -385,23 +416,69 @@ def measure_variants(lb, dev, stream, dist, steps):
     return out
 
 
-def cpu_baseline(w, seconds=10.0):
-    """The oracle, as it stands, on a bounded sample of the headline workload."""
+def host_cpu():
+    """Host cores this process may use, and the CPU model as /proc/cpuinfo names it."""
+    try:
+        cores = len(os.sched_getaffinity(0))
+    except AttributeError:
+        cores = os.cpu_count() or 1
+    model = platform.machine()
+    try:
+        info = open("/proc/cpuinfo").read()
+        m = re.search(r"^model name\s*:\s*(.+)$", info, re.M)
+        if m:
+            model = m.group(1).strip()
+        else:
+            imp = re.search(r"^CPU implementer\s*:\s*(\S+)$", info, re.M)
+            part = re.search(r"^CPU part\s*:\s*(\S+)$", info, re.M)
+            if imp and part:
+                model = f"{platform.machine()} implementer {imp.group(1)} part {part.group(1)}"
+    except OSError:
+        pass
+    return cores, model
+
+
+def oracle_rate(w, threads, seconds, rows_per_thread):
+    """Tokens/s of the oracle, as it stands, on the headline workload's rows: `threads`
+    threads each run oracle calls on their own block of `rows_per_thread` rows until
+    `seconds` have passed (the oracle releases the GIL inside its C code)."""
     import oracle
     oracle._load()
-    rows = min(w.T, 64)
-    P = [p[:rows] for p in w.partials]
-    R = w.residual[:rows]
-    n, t0 = 0, time.perf_counter()
-    while True:
-        oracle.fold_norm(P, R, w.gamma, w.eps, want_y=False, want_fp8=True)
-        n += 1
-        el = time.perf_counter() - t0
-        if el >= seconds:
-            break
-    return {"value": round(n * rows / el, 1), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{n} single-threaded oracle calls on the first {rows} rows of the "
-                      f"K=4 T=2048 H=4096 prefill workload ({el:.1f} s)"}
+    blocks = []
+    for i in range(threads):
+        lo = (i * rows_per_thread) % w.T
+        hi = min(w.T, lo + rows_per_thread)
+        blocks.append(([p[lo:hi] for p in w.partials], w.residual[lo:hi]))
+    t0 = time.perf_counter()
+    stop = t0 + seconds
+
+    def work(block):
+        P, R = block
+        n = 0
+        while time.perf_counter() < stop:
+            oracle.fold_norm(P, R, w.gamma, w.eps, want_y=False, want_fp8=True)
+            n += R.shape[0]
+        return n
+
+    with concurrent.futures.ThreadPoolExecutor(threads) as ex:
+        done = sum(ex.map(work, blocks))
+    el = time.perf_counter() - t0
+    return done / el, done, el
+
+
+def cpu_baseline(w, seconds=10.0):
+    """The oracle, as it stands, on a bounded sample of the headline workload: rows
+    partitioned over every host core (the reported value), and on one core."""
+    cores, model = host_cpu()
+    rows = 16
+    v1, n1, e1 = oracle_rate(w, 1, seconds / 3, rows)
+    vn, nn, en = oracle_rate(w, cores, seconds, rows)
+    return {"value": round(vn, 1), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{nn} rows of the K=4 T=2048 H=4096 prefill workload (FP8 read), "
+                      f"{rows}-row blocks, one per thread, over {cores} threads for "
+                      f"{en:.1f} s",
+            "single_thread": {"value": round(v1, 1), "rows": n1, "seconds": round(e1, 1)},
+            "cpu": model}
 
 
 def run_native(args, dist):
@@ -519,24 +596,36 @@ def run_reference(args, dist):
     import oracle
     oracle._load()
     w = wl.prefill_fold_norm_fp8()
-    # calibrate, then size each step's sample so the whole run takes ~2 minutes
+    cores, model = host_cpu()
+    # calibrate, then size each step's sample so the whole run takes ~2 minutes with
+    # the step's rows split into one contiguous block per host core
     t0 = time.perf_counter()
     oracle.fold_norm([p[:8] for p in w.partials], w.residual[:8], w.gamma, w.eps,
                      want_y=False, want_fp8=True)
     per_row = (time.perf_counter() - t0) / 8
     budget = 120.0
-    rows = int(max(1, min(w.T, budget / max(1, args.steps + args.warmup) / per_row)))
-    P = [p[:rows] for p in w.partials]
-    R = w.residual[:rows]
-    for _ in range(args.warmup):
-        oracle.fold_norm(P, R, w.gamma, w.eps, want_y=False, want_fp8=True)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        oracle.fold_norm(P, R, w.gamma, w.eps, want_y=False, want_fp8=True)
-    el = time.perf_counter() - t0
+    rows = int(budget / max(1, args.steps + args.warmup) / per_row * cores)
+    rows = max(cores, min(w.T, rows))
+    edges = [rows * i // cores for i in range(cores + 1)]
+    blocks = [([p[lo:hi] for p in w.partials], w.residual[lo:hi])
+              for lo, hi in zip(edges[:-1], edges[1:]) if hi > lo]
+
+    def one(block):
+        oracle.fold_norm(block[0], block[1], w.gamma, w.eps, want_y=False, want_fp8=True)
+
+    with concurrent.futures.ThreadPoolExecutor(len(blocks)) as ex:
+        def step():
+            for _ in ex.map(one, blocks):
+                pass
+        for _ in range(args.warmup):
+            step()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            step()
+        el = time.perf_counter() - t0
     value = rows * args.steps / el
-    sample = (f"{rows} rows of the K=4 T=2048 H=4096 prefill workload per step, "
-              f"single-threaded oracle")
+    sample = (f"{rows} rows of the K=4 T=2048 H=4096 prefill workload per step, split "
+              f"into {len(blocks)} row blocks run by {len(blocks)} threads")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
         "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
@@ -545,8 +634,8 @@ def run_reference(args, dist):
         "data": "synthetic (seeded normal bf16 inputs)",
         "config": {"workload": HEADLINE, "K": w.K, "T": w.T, "H": w.H, "eps": w.eps,
                    "rows_per_step": rows},
-        "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": 1,
-                         "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": len(blocks),
+                         "kind": "oracle", "sample": sample, "cpu": model},
         "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

@@ -65,7 +65,10 @@ def test_reference_arm_prints_the_contract_line():
         assert key in line
     assert line["impl"] == "reference" and line["steps"] == 4
     assert line["config"]["workload"] == "prefill_fold_norm_fp8"
-    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    cores = len(os.sched_getaffinity(0))
+    assert line["cpu_baseline"]["kind"] == "oracle"
+    assert 1 <= line["cpu_baseline"]["cores"] <= cores
+    assert line["config"]["rows_per_step"] >= line["cpu_baseline"]["cores"]
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
 
 
@@ -84,3 +87,16 @@ def test_native_arm_refuses_to_run_without_a_gpu():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--steps", "4"],
                        capture_output=True, text=True, timeout=300, cwd=ROOT)
     assert r.returncode != 0 and "needs a CUDA GPU" in (r.stderr + r.stdout)
+
+
+def test_oracle_rate_counts_every_thread():
+    """The CPU baseline's row-partitioned oracle timing counts the rows of every
+    thread and reports a positive rate."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from layer_boundary_fusion_gb300 import workloads as wl
+    w = wl.tiny_fold_norm()
+    rate, rows, el = bench.oracle_rate(w, 2, 0.2, 8)
+    assert rows > 0 and rows % 8 == 0 and rate == rows / el
+    cores, model = bench.host_cpu()
+    assert cores >= 1 and model

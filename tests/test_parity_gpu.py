@@ -15,7 +15,7 @@ import torch
 import oracle
 from layer_boundary_fusion_gb300 import workloads as wl
 from parity_util import (Guarded, assert_bf16_close, assert_bits_equal, assert_fp8_close,
-                         dev_bits, host_bits, SENTINEL16)
+                         dev_bits, f32, host_bits, SENTINEL16)
 
 pytestmark = pytest.mark.gpu
 
@@ -222,7 +222,8 @@ def test_moe_finalize_fp8_and_initial(lb):
 
 
 @pytest.mark.parametrize("T,H,E,topk", [(1, 4096, 16, 16), (37, 520, 8, 3), (64, 8192, 64, 8),
-                                        (5, 16384, 8, 1)])
+                                        (5, 16384, 8, 1), (200, 1024, 16, 16),
+                                        (1, 2048, 128, 8)])
 def test_moe_shapes(lb, T, H, E, topk):
     w = wl.moe_workload("m", T, H, E, topk, seed=T + H)
     want = oracle.moe_finalize_fold_norm(w.expert_out, w.idx, w.w, w.residual, w.gamma, w.eps)
@@ -383,6 +384,8 @@ def test_specified_workloads_take_the_intended_kernels(lb):
     (8, 152, 2048),
     (2, 160, 4096),     # stream kernel, one or two rows per CTA
     (4, 1000, 4096),    # stream kernel
+    (16, 300, 1024),    # stream kernel at the maximum K (17 staged rows per stage)
+    (1, 2, 131072),     # the largest hidden size: a row split over an 8-CTA cluster
 ])
 def test_shapes(lb, K, T, H):
     w = wl.fold_workload("shape", K, T, H, seed=K * 1000 + T + H)
@@ -571,3 +574,38 @@ def test_host_pipeline_matches_the_oracle(lb):
         torch.cuda.synchronize()
         assert_bits_equal(ro.numpy().view(np.uint16), want["residual_out"], f"host residual' {call}")
         assert_fp8_close(q.numpy(), want["q"], sc.numpy(), want["scale"], f"host fp8 {call}")
+
+
+def test_non_finite_inputs_propagate_like_the_oracle(lb):
+    """A NaN or an infinity in a partial makes its row's outputs non-finite where the
+    definition says so; other rows are unaffected.  Compared as float values
+    (NaN == NaN), since NaN payloads need not match."""
+    w = wl.fold_workload("nan", 2, 200, 1024, seed=96)
+    P = [p.copy() for p in w.partials]
+    P[0][3, 10] = 0x7FC0                      # NaN
+    P[1][7, 20] = 0x7F80                      # +inf
+    P[1][9, 30] = 0xFF80                      # -inf
+    P[0][9, 30] = 0x7F80                      # +inf + -inf = NaN
+    want = oracle.fold_norm(P, w.residual, w.gamma, w.eps)
+    for T in (200, 100):                      # stream kernel, row kernel
+        got = gpu_fold(lb, [p[:T] for p in P], w.residual[:T], w.gamma, w.eps)
+        for k in ("residual_out", "y"):
+            g = f32(got[k]).astype(np.float64)
+            e = f32(want[k][:T]).astype(np.float64)
+            assert np.array_equal(np.isnan(g), np.isnan(e)), k
+            fin = np.isfinite(e)
+            assert np.array_equal(np.isinf(g), np.isinf(e)), k
+            assert np.all(g[np.isinf(e)] == e[np.isinf(e)])
+            assert np.all(np.abs(g[fin] - e[fin]) <= 1e-2 * np.abs(e[fin]) + 1e-3), k
+
+
+def test_unfused_two_call_path_matches_the_oracle(lb):
+    """The unfused fallback the benchmark compares against (the completed sum written
+    to a bf16 buffer, then residual add + RMSNorm of that buffer) computes what the
+    oracle computes for the same two calls."""
+    w = wl.fold_workload("unfused", 4, 300, 4096, seed=97)
+    s_want = oracle.fold_norm(w.partials, None, None, w.eps, want_y=False)["residual_out"]
+    want = oracle.fold_norm([s_want], w.residual, w.gamma, w.eps)
+    s_got = gpu_fold(lb, w.partials, None, w.gamma, w.eps, want_y=False)["residual_out"]
+    assert_bits_equal(s_got, s_want, "unfused sum")
+    check_fold(gpu_fold(lb, [s_got], w.residual, w.gamma, w.eps), want, "unfused add+norm")
