@@ -307,8 +307,9 @@ bool choose_stream_shape(int64_t rows, int64_t H, int n_inputs, int num_sms,
     int64_t per_cta = LB_SMEM_PER_SM / LB_STREAM_CTAS_PER_SM - 1024;
     if (per_cta > smem_per_block)
         per_cta = smem_per_block;
-    // per stage: its input rows, two mbarriers and an 80-byte metadata block
-    int64_t ns = (per_cta - reserve) / (stage + 96);
+    // per stage: its input rows, two mbarriers and two row-metadata blocks
+    const int64_t per_stage = stage + 16 + 2 * LB_STREAM_META_BYTES;
+    int64_t ns = (per_cta - reserve) / per_stage;
     if (ns > LB_STREAM_MAX_STAGES)
         ns = LB_STREAM_MAX_STAGES;
     if (ns < 2)
@@ -336,7 +337,7 @@ bool choose_stream_shape(int64_t rows, int64_t H, int n_inputs, int num_sms,
     out->consumer_warps = ncw;
     out->vpt = static_cast<int>(vpt);
     out->stages = static_cast<int>(ns);
-    out->smem_bytes = static_cast<int>(ns * (stage + 96));
+    out->smem_bytes = static_cast<int>(ns * per_stage);
     return true;
 }
 

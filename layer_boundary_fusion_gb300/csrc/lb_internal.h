@@ -27,6 +27,14 @@
 #ifndef LB_STREAM_MAX_STAGES
 #define LB_STREAM_MAX_STAGES 8
 #endif
+// MoE finalize: rows of routing metadata (indices, weights) the stream kernel's
+// producer fetches ahead of the row it issues (at most the stage count).
+#ifndef LB_MOE_META_AHEAD
+#define LB_MOE_META_AHEAD 2
+#endif
+// Bytes of one row-metadata block of the stream kernel (MoE expert indices, routing
+// weights, valid mask); the kernel keeps two blocks per stage.
+#define LB_STREAM_META_BYTES 144
 // Shared memory of one SM (GB300: 228 KB), shared by the CTAs resident on it.
 #ifndef LB_SMEM_PER_SM
 #define LB_SMEM_PER_SM 233472

@@ -125,6 +125,31 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         : "memory");
 }
 
+// 4 bytes global -> shared by the issuing thread (cp.async), in the thread's current
+// group; the copy is complete for that thread after a wait covering its group.
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Wait until at most `n` of this thread's committed groups are pending (n <= 7;
+// larger n waits for all of them).
+__device__ __forceinline__ void cp_async_wait_pending(int n) {
+    switch (n) {
+    case 7: asm volatile("cp.async.wait_group 7;" ::: "memory"); break;
+    case 6: asm volatile("cp.async.wait_group 6;" ::: "memory"); break;
+    case 5: asm volatile("cp.async.wait_group 5;" ::: "memory"); break;
+    case 4: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
+    case 3: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+    case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+    case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+    default: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+    }
+}
+
 // ------------------------------------------------------------------------------------
 // Row schedule shared by producer and consumers
 // ------------------------------------------------------------------------------------
@@ -160,11 +185,12 @@ __device__ __forceinline__ int64_t advance(const Params &p, int64_t row, int n) 
 // ------------------------------------------------------------------------------------
 
 struct StageMeta {
+    int32_t idx[LB_MAX_TOPK];
     float w[LB_MAX_TOPK];
     uint32_t valid;
     uint32_t pad[3];
 };
-static_assert(sizeof(StageMeta) == 80, "stage metadata size");
+static_assert(sizeof(StageMeta) == LB_STREAM_META_BYTES, "stage metadata size");
 
 // Threads per CTA the kernel is compiled for: one producer warp plus the consumer
 // groups.  Four-vector threads need more registers and run one group.
@@ -191,7 +217,8 @@ __device__ __forceinline__ bool group_sync_or(bool pred, int id, int nthreads) {
 }
 
 // Shared-memory layout (dynamic): [stages][slot][slot_bytes], the mbarriers (full,
-// empty), then one StageMeta per stage.
+// empty), then a ring of 2 x stages StageMeta blocks: row i's metadata is in block
+// i % (2 stages), fetched up to `stages` rows before row i is issued.
 // Slot j < n_main holds partial j (fold) or routed row j (MoE); the residual row, if
 // any, is slot n_main.  The CTA's rows are numbered i = 0, 1, ... in the order the
 // producer streams them; stage i % stages holds row i, and consumer group i % groups
@@ -221,8 +248,11 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
     const uint32_t full0 = smem_addr(bars);
     const uint32_t empty0 = smem_addr(bars + ns);
     const uint32_t stage0 = smem_addr(smem);
-    // MoE: per stage, the row's routing weights and the mask of valid expert indices,
-    // written by the producer before it arms the stage's "full" barrier.
+    // MoE: per row, its expert indices and routing weights (cp.async by the producer,
+    // d <= ns rows ahead) and the mask of valid indices (written before the producer
+    // arms the stage's "full" barrier).  Row i uses block i % (2 ns): the block of row
+    // i + d last served row i + d - 2 ns, whose stage has since been released and
+    // reissued (row i + d - ns < i), so it is free when the fetch is issued.
     StageMeta *meta = reinterpret_cast<StageMeta *>(bars + 2 * ns);
 
     if (G < 1 || ns % G != 0) {                           // launch contract, see above
@@ -266,14 +296,27 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
         const int64_t rows = p.rows;
         int64_t row = next_row(p, blockIdx.x);
         pdl_wait();
-        // MoE: each lane < topk holds the expert row of its slot, loaded one row ahead
-        // so that the index latency hides behind the wait for a free stage.
-        int32_t e_next = -1;
-        float w_next = 0.0f;
-        if (kMode == kMoe && lane < n_main && row < rows) {
-            e_next = __ldg(idx + row * topk + lane);
-            w_next = __ldg(p.w + row * topk + lane);
-        }
+        // MoE: lane j < topk fetches slot j's index and weight of a row into the row's
+        // metadata block, one cp.async group per row, LB_MOE_META_AHEAD rows ahead of
+        // its issue, so that no index load sits between a free stage and its copies
+        // (the first rows' metadata is fetched at once).  Two rows ahead measured
+        // faster than one (the load latency under a saturated memory system outlasts
+        // a row) and than a full ring of stages ahead.
+        int64_t ahead = row;             // next row whose metadata is fetched
+        auto fetch_meta = [&](int blk) {
+            if (kMode != kMoe)
+                return;
+            if (lane < n_main && ahead < rows) {
+                cp_async4(smem_addr(&meta[blk].idx[lane]), idx + ahead * topk + lane);
+                cp_async4(smem_addr(&meta[blk].w[lane]), p.w + ahead * topk + lane);
+            }
+            cp_async_commit();
+            if (ahead < rows)
+                ahead = next_row(p, ahead + gridDim.x);
+        };
+        const int ahead_rows = ns < LB_MOE_META_AHEAD ? ns : LB_MOE_META_AHEAD;
+        for (int b = 0; b < ahead_rows; ++b)
+            fetch_meta(b);
         int s = 0;                       // stage of the next row to issue
         uint32_t k = 0;                  // use of that stage
         for (; row < rows; ++issued) {
@@ -285,21 +328,22 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
                 break;
             }
             const uint32_t full = full0 + 8 * s;
+            const int blk = s + ns * static_cast<int>(k & 1u);
             // sources of this row: lane j handles slot j (n_slots <= 17 <= 32)
             const void *src = nullptr;
             if (kMode == kMoe && lane < n_main) {
-                if (e_next >= 0 && static_cast<int64_t>(e_next) < n_experts)
-                    src = experts + static_cast<int64_t>(e_next) * H;
+                cp_async_wait_pending(ahead_rows - 1);   // this row's group landed
+                const int32_t e = meta[blk].idx[lane];
+                if (e >= 0 && static_cast<int64_t>(e) < n_experts)
+                    src = experts + static_cast<int64_t>(e) * H;
             } else if (lane_base != nullptr) {
                 src = lane_base + (lane_row0 + row) * H;
             }
             const unsigned valid = __ballot_sync(0xFFFFFFFFu, src != nullptr);
             if (kMode == kMoe) {
-                if (lane < n_main)
-                    meta[s].w[lane] = w_next;
                 if (lane == 0) {
                     const unsigned main_mask = (n_main >= 32) ? 0xFFFFFFFFu : ((1u << n_main) - 1u);
-                    meta[s].valid = valid & main_mask;
+                    meta[blk].valid = valid & main_mask;
                     if ((valid & main_mask) != main_mask && p.bad_index != nullptr)
                         *p.bad_index = 1;
                 }
@@ -315,15 +359,14 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
                     bulk_g2s(dst + j * slot_bytes, sj, slot_bytes, full);
             }
             row = next_row(p, row + gridDim.x);
-            if (kMode == kMoe && lane < n_main && row < rows) {
-                e_next = __ldg(idx + row * topk + lane);
-                w_next = __ldg(p.w + row * topk + lane);
-            }
+            fetch_meta((issued + ahead_rows) % (2 * ns));   // block of row i + ahead_rows
             if (++s == ns) {
                 s = 0;
                 ++k;
             }
         }
+        if (kMode == kMoe)
+            cp_async_wait_pending(0);    // no metadata copy outlives the CTA
         if (!ok && lane == 0) {
             atomicOr(&g_device_error, kDeviceErrTimeout);
             abort_flag = 1;
@@ -394,6 +437,7 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
             phase ^= 1u;
         }
         const uint32_t k = phase;
+        const int blk = s + ns * static_cast<int>(phase);   // this row's metadata block
 
         // A thread whose wait fails reads nothing from the stage and writes nothing;
         // the group learns of it at its row barrier and leaves together.
@@ -409,14 +453,14 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
                 acc[v][e] = make_float2(0.0f, 0.0f);
         if (ok) {
             const uint32_t stage = stage0 + static_cast<uint32_t>(s) * stage_bytes;
-            const uint32_t valid = (kMode == kMoe) ? meta[s].valid : 0u;
+            const uint32_t valid = (kMode == kMoe) ? meta[blk].valid : 0u;
 #pragma unroll
             for (int j = 0; j < LB_MAX_K; ++j) {
                 if (j >= n_main)
                     break;
                 if (kMode == kMoe && !((valid >> j) & 1u))
                     continue;
-                const float wj = (kMode == kMoe) ? meta[s].w[j] : 1.0f;
+                const float wj = (kMode == kMoe) ? meta[blk].w[j] : 1.0f;
                 const uint32_t slot = stage + static_cast<uint32_t>(j) * slot_bytes;
 #pragma unroll
                 for (int v = 0; v < kVpt; ++v)

@@ -67,18 +67,18 @@ SMEM = 232448          # opt-in shared memory per CTA on GB300
 
 @pytest.mark.parametrize("rows,H,n_in,plan", [
     # (kernel, grid, threads, vectors/thread, ctas/row, stages, smem)
-    (2048, 4096, 5, (1, 152, 800, 2, 1, 3, 123168)),    # prefill K=4 + residual: stream
-    (1024, 4096, 9, (1, 152, 800, 2, 1, 3, 221472)),    # MoE top-8 + residual: stream
-    (254, 4096, 9, (1, 152, 800, 2, 1, 3, 221472)),     # one ragged slice: stream
+    (2048, 4096, 5, (1, 152, 800, 2, 1, 3, 123792)),    # prefill K=4 + residual: stream
+    (1024, 4096, 9, (1, 152, 800, 2, 1, 3, 222096)),    # MoE top-8 + residual: stream
+    (254, 4096, 9, (1, 152, 800, 2, 1, 3, 222096)),     # one ragged slice: stream
     (64, 4096, 9, (0, 64, 512, 1, 1, 0, 0)),            # decode: row kernel, a CTA per row
     (1, 4096, 2, (0, 1, 512, 1, 1, 0, 0)),
     (16, 512, 3, (0, 16, 64, 1, 1, 0, 0)),              # tiny: one CTA per row
-    (4096, 8192, 5, (1, 152, 288, 4, 1, 2, 164032)),
+    (4096, 8192, 5, (1, 152, 288, 4, 1, 2, 164448)),
     (4096, 8192, 9, (0, 4096, 512, 2, 1, 0, 0)),        # no double-buffered stage fits
     (4096, 16384, 3, (0, 4096, 512, 4, 1, 0, 0)),
     (4096, 32768, 2, (0, 8192, 512, 4, 2, 0, 0)),
-    (4096, 520, 2, (1, 152, 416, 1, 1, 6, 13056)),      # 65 vectors: partly active warp
-    (4096, 8, 2, (1, 152, 224, 1, 1, 6, 768)),
+    (4096, 520, 2, (1, 152, 416, 1, 1, 6, 14304)),      # 65 vectors: partly active warp
+    (4096, 8, 2, (1, 152, 224, 1, 1, 6, 2016)),
 ])
 def test_launch_plan(lib, rows, H, n_in, plan):
     p = lib.lb_launch_plan(rows, H, n_in, 152, SMEM)
@@ -108,7 +108,7 @@ def test_launch_plan_covers_every_row_vector(lib):
                     assert 2 <= p.stages <= 8 and p.grid == min(rows, 152)
                     # every stage belongs to one consumer group
                     assert p.stages % groups == 0
-                    assert p.smem_bytes == p.stages * (n_in * H * 2 + 96)
+                    assert p.smem_bytes == p.stages * (n_in * H * 2 + 16 + 2 * 144)
                     assert p.smem_bytes + 1024 <= SMEM
                 assert p.vectors_per_thread in (1, 2, 4)
 
