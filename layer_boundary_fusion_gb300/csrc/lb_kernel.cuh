@@ -85,6 +85,28 @@ __device__ __forceinline__ void unpack8x2(const uint4 &w, float2 f[4]) {
     f[3] = make_float2(__uint_as_float(w.w << 16), __uint_as_float(w.w & 0xFFFF0000u));
 }
 
+// acc += the 8 bf16 values of w (element 2e in acc[e].x, 2e+1 in acc[e].y), each add
+// one mixed-precision add.rn.f32.bf16: the bf16 operand widens exactly, so every add
+// rounds like the binary32 add of the definition, in one instruction per element.
+__device__ __forceinline__ void add_bf16x8(float2 acc[4], const uint4 &w) {
+    asm("{\n\t.reg .b16 l0, h0, l1, h1, l2, h2, l3, h3;\n\t"
+        "mov.b32 {l0, h0}, %8;\n\t"
+        "mov.b32 {l1, h1}, %9;\n\t"
+        "mov.b32 {l2, h2}, %10;\n\t"
+        "mov.b32 {l3, h3}, %11;\n\t"
+        "add.rn.f32.bf16 %0, l0, %0;\n\t"
+        "add.rn.f32.bf16 %1, h0, %1;\n\t"
+        "add.rn.f32.bf16 %2, l1, %2;\n\t"
+        "add.rn.f32.bf16 %3, h1, %3;\n\t"
+        "add.rn.f32.bf16 %4, l2, %4;\n\t"
+        "add.rn.f32.bf16 %5, h2, %5;\n\t"
+        "add.rn.f32.bf16 %6, l3, %6;\n\t"
+        "add.rn.f32.bf16 %7, h3, %7;\n\t}"
+        : "+f"(acc[0].x), "+f"(acc[0].y), "+f"(acc[1].x), "+f"(acc[1].y),
+          "+f"(acc[2].x), "+f"(acc[2].y), "+f"(acc[3].x), "+f"(acc[3].y)
+        : "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w));
+}
+
 __device__ __forceinline__ uint4 pack8x2(const float2 f[4]) {
     return make_uint4(pack_bf16x2(f[0].x, f[0].y), pack_bf16x2(f[1].x, f[1].y),
                       pack_bf16x2(f[2].x, f[2].y), pack_bf16x2(f[3].x, f[3].y));
@@ -255,11 +277,15 @@ __global__ void __launch_bounds__(512, 1) boundary_kernel(const __grid_constant_
 #pragma unroll
                     for (int i = 0; i < kVpt; ++i)
                         if (act[i]) {
-                            float2 f[4];
-                            unpack8x2(buf[kk][i], f);
+                            if (kVpt >= 4) {       // (keeps the 4-vector variant unspilled)
+                                float2 f[4];
+                                unpack8x2(buf[kk][i], f);
 #pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                acc[i][e] = __fadd2_rn(acc[i][e], f[e]);
+                                for (int e = 0; e < 4; ++e)
+                                    acc[i][e] = __fadd2_rn(acc[i][e], f[e]);
+                            } else {
+                                add_bf16x8(acc[i], buf[kk][i]);
+                            }
                         }
                 }
         }
@@ -310,13 +336,8 @@ __global__ void __launch_bounds__(512, 1) boundary_kernel(const __grid_constant_
     if (has_res) {
 #pragma unroll
         for (int i = 0; i < kVpt; ++i)
-            if (act[i]) {
-                float2 f[4];
-                unpack8x2(rv[i], f);
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    acc[i][e] = __fadd2_rn(acc[i][e], f[e]);
-            }
+            if (act[i])
+                add_bf16x8(acc[i], rv[i]);
     }
     if (p.residual_out != nullptr || p.snapshot != nullptr) {
 #pragma unroll

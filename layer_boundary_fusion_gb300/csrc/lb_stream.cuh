@@ -80,29 +80,45 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return done != 0;
 }
 
+// As mbar_try_wait, but the thread may stay suspended in the instruction until the
+// phase completes or about `hint_ns` have passed: a waiter then issues a handful of
+// instructions per wait instead of polling, leaving the SM's issue slots to the
+// warps that are working.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity,
+                                                      uint32_t hint_ns) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return done != 0;
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
 
-// Bounded wait for the phase with the given parity: at most 2^24 polls and about one
-// second.  `abort_flag` (shared) is polled too, so a waiter gives up early once
-// another warp of the CTA has given up.  Returns false on time-out or abort.
+// Bounded wait for the phase with the given parity: at most 2^24 suspending waits of
+// up to 20 us each and about one second in all.  `abort_flag` (shared) is read after
+// every wait, so a waiter gives up early once another warp of the CTA has given up.
+// Returns false on time-out or abort.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   const volatile int *abort_flag) {
     if (mbar_try_wait(bar, parity))
         return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 0; it < (1u << 24); ++it) {
-        if (mbar_try_wait(bar, parity))
+        if (mbar_try_wait_suspend(bar, parity, 20000u))
             return true;
-        if ((it & 255u) == 255u) {
-            if (abort_flag != nullptr && *abort_flag)
-                return false;
-            if (global_timer_ns() - t0 > 1000000000ull)
-                return false;
-        }
+        if (abort_flag != nullptr && *abort_flag)
+            return false;
+        if (global_timer_ns() - t0 > 1000000000ull)
+            return false;
     }
     return false;
 }
@@ -465,25 +481,24 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
 #pragma unroll
                 for (int v = 0; v < kVpt; ++v)
                     if (act[v]) {
-                        float2 f[4];
-                        unpack8x2(lds128(slot + soff[v]), f);
+                        const uint4 x = lds128(slot + soff[v]);
+                        if (kMode == kMoe) {
+                            float2 f[4];
+                            unpack8x2(x, f);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            acc[v][e] = (kMode == kMoe) ? add_mul2_rn(acc[v][e], wj, f[e])
-                                                        : __fadd2_rn(acc[v][e], f[e]);
+                            for (int e = 0; e < 4; ++e)
+                                acc[v][e] = add_mul2_rn(acc[v][e], wj, f[e]);
+                        } else {
+                            add_bf16x8(acc[v], x);
+                        }
                     }
             }
             if (has_res) {
                 const uint32_t slot = stage + static_cast<uint32_t>(n_main) * slot_bytes;
 #pragma unroll
                 for (int v = 0; v < kVpt; ++v)
-                    if (act[v]) {
-                        float2 f[4];
-                        unpack8x2(lds128(slot + soff[v]), f);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            acc[v][e] = __fadd2_rn(acc[v][e], f[e]);
-                    }
+                    if (act[v])
+                        add_bf16x8(acc[v], lds128(slot + soff[v]));
             }
         }
         // the stage's data is in registers: hand it back to the producer
