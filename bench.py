@@ -99,9 +99,12 @@ def bytes_fold(K, rows, H, residual=True, res_out=True, y=True, fp8=False):
     return b
 
 
-def bytes_moe(T, H, topk, residual=True):
-    return (T * topk * H * 2 + 2 * T * topk * 4 + (T * H * 2 if residual else 0) + H * 4
-            + 2 * T * H * 2)
+def bytes_moe(T, H, topk, residual=True, y=True, fp8=False):
+    b = T * topk * H * 2 + 2 * T * topk * 4 + (T * H * 2 if residual else 0) + H * 4
+    b += T * H * 2 * (1 + (1 if y else 0))
+    if fp8:
+        b += T * H + T * 4
+    return b
 
 
 # --------------------------------------------------------------------------------------
@@ -342,7 +345,18 @@ def measure_variants(lb, dev, stream, dist, steps):
     el, _ = time_graph(ls, steps, 20, stream, dist)
     record("ragged_slice", v, nb, el, steps, plan_of(lb, S, w.H, w.K + 1, props),
            f"rotated {ns} sets")
-    del sets, ls, P0
+    # the same slice with the FP8 read
+    nb8 = bytes_fold(w.K, v, w.H, y=False, fp8=True)
+    Q = [(torch.empty((S, w.H), dtype=torch.uint8, device=dev),
+          torch.empty((S,), dtype=torch.float32, device=dev)) for _ in sets]
+    ls = [(lambda s=s, q=q: lb.lb_slice_fold_norm(s[0], w.T_pad, w.num_slices, w.slice,
+                                                 w.set_offsets, w.set_counts, s[1], s[2], G,
+                                                 None, q[0], q[1], w.H, w.eps, stream=sp))
+          for s, q in zip(sets, Q)]
+    el, _ = time_graph(ls, steps, 20, stream, dist)
+    record("ragged_slice_fp8", v, nb8, el, steps, plan_of(lb, S, w.H, w.K + 1, props),
+           f"rotated {ns} sets")
+    del sets, ls, P0, Q
     # variable-size reduce-scatter (rsv): ranks 1 (512 rows) and 3 (1470 rows)
     for rank in (1, 3):
         o, c = int(w.set_offsets[rank]), int(w.set_counts[rank])
@@ -375,6 +389,38 @@ def measure_variants(lb, dev, stream, dist, steps):
     el, _ = time_graph(ls, steps, 20, stream, dist)
     record("moe_finalize", w.T, nb, el, steps, plan_of(lb, w.T, w.H, w.topk + 1, props),
            f"rotated {ns} sets")
+    # the terminal handoff: the same finalize feeding a Gemma final norm (1 + gamma)
+    ls = [(lambda s=s: lb.lb_moe_finalize_fold_norm(s[0], w.expert_out.shape[0], I, Wt, w.topk,
+                                                   s[1], s[2], G, s[3], None, None, w.T, w.H,
+                                                   w.eps, None, stream=sp, gemma=True))
+          for s in sets]
+    el, _ = time_graph(ls, steps, 20, stream, dist)
+    record("moe_finalize_gemma", w.T, nb, el, steps, plan_of(lb, w.T, w.H, w.topk + 1, props),
+           f"rotated {ns} sets")
+    # the FP8 read on the finalize (codes + scales instead of the bf16 read)
+    nb8 = bytes_moe(w.T, w.H, w.topk, y=False, fp8=True)
+    Q = [(torch.empty((w.T, w.H), dtype=torch.uint8, device=dev),
+          torch.empty((w.T,), dtype=torch.float32, device=dev)) for _ in sets]
+    ls = [(lambda s=s, q=q: lb.lb_moe_finalize_fold_norm(
+        s[0], w.expert_out.shape[0], I, Wt, w.topk, s[1], s[2], G, None, q[0], q[1], w.T, w.H,
+        w.eps, None, stream=sp)) for s, q in zip(sets, Q)]
+    el, _ = time_graph(ls, steps, 20, stream, dist)
+    record("moe_finalize_fp8", w.T, nb8, el, steps, plan_of(lb, w.T, w.H, w.topk + 1, props),
+           f"rotated {ns} sets")
+    del sets, ls, Q
+    # the headline call with the Gemma weight and an owned snapshot of residual'
+    w = wl.prefill_fold_norm_fp8()
+    nb = bytes_fold(w.K, w.T, w.H, fp8=True, y=False) + w.T * w.H * 2
+    ns = n_sets(nb, dev)
+    sets = fold_sets(w, dev, ns, True)
+    for s in sets:
+        s.snap = torch.empty_like(s.ro)
+    ls = [(lambda s=s: lb.lb_fold_norm_fp8(s.P, s.R, s.ro, s.G, s.qo, s.so, None, w.T, w.H,
+                                          w.eps, stream=sp, gemma=True,
+                                          residual_snapshot=s.snap)) for s in sets]
+    el, _ = time_graph(ls, steps, 20, stream, dist)
+    record("prefill_fp8_gemma_snapshot", w.T, nb, el, steps,
+           plan_of(lb, w.T, w.H, w.K + 1, props), f"rotated {ns} sets")
     del sets, ls
     # fusion gain: the same fold + bf16 read as one fused call and as the unfused
     # fallback of two calls (the completed sum written to a bf16 buffer, then residual

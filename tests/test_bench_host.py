@@ -22,6 +22,8 @@ def test_algorithmic_bytes_of_the_specified_workloads():
     assert bench.bytes_fold(8, 64, 4096, residual=False) == 5_259_264
     assert bench.bytes_fold(8, 254, 4096) == 22_904_832
     assert bench.bytes_moe(1024, 4096, 8) == 92_356_608
+    # FP8 read on the finalize: residual' + codes + scales instead of residual' + y
+    assert bench.bytes_moe(1024, 4096, 8, y=False, fp8=True) == 88_166_400
     assert bench.bytes_fold(2, 16, 512) == 83_968
 
 
