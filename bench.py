@@ -229,9 +229,13 @@ def kernel_name(plan, mode, fp8):
 
 
 def kernel_source_hash():
+    """Hash of the sources the kernels are compiled from (device code and its launch
+    parameters; the host-only API files are left out)."""
     h = hashlib.sha256()
-    files = sorted(glob.glob(os.path.join(ROOT, "layer_boundary_fusion_gb300", "csrc", "*")))
-    for f in files + [os.path.join(ROOT, "include", "lb.h")]:
+    csrc = os.path.join(ROOT, "layer_boundary_fusion_gb300", "csrc")
+    files = sorted(glob.glob(os.path.join(csrc, "*.cuh")) +
+                   [os.path.join(csrc, n) for n in ("lb_fold.cu", "lb_moe.cu", "lb_internal.h")])
+    for f in files:
         h.update(os.path.basename(f).encode())
         h.update(open(f, "rb").read())
     return h.hexdigest()

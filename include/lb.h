@@ -62,7 +62,12 @@ typedef enum {
     LB_ERR_INVALID_ARGUMENT = 1, /* NULL where a buffer is required, bad sizes, overlap */
     LB_ERR_MISALIGNED = 2,       /* a tensor pointer is not 16-byte aligned */
     LB_ERR_UNSUPPORTED = 3,      /* K, topk, sets or H outside the supported range */
-    LB_ERR_CUDA = 4              /* the CUDA launch failed; see lb_last_cuda_error() */
+    LB_ERR_CUDA = 4,             /* the CUDA launch failed; see lb_last_cuda_error() */
+    /* residual stream misuse (lb_residual.h; "Layer boundaries", section "Integration
+     * checklist and common errors") */
+    LB_ERR_NOT_STARTED = 5,      /* start the layer stack before entering a stage */
+    LB_ERR_FOREIGN_OUTPUT = 6,   /* the output does not belong to this residual stream */
+    LB_ERR_UPDATE_PENDING = 7    /* write the residual update before taking the output */
 } lb_status;
 
 /* Static, human-readable name of a status. */

@@ -38,7 +38,7 @@ def sources():
 
 def _inputs():
     return sources() + glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(
-        os.path.join(CSRC, "*.cuh")) + [os.path.join(INCLUDE, "lb.h"), __file__]
+        os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h")) + [__file__]
 
 
 def up_to_date() -> bool:

@@ -380,6 +380,9 @@ const char *lb_status_string(lb_status status) {
     case LB_ERR_MISALIGNED: return "LB_ERR_MISALIGNED";
     case LB_ERR_UNSUPPORTED: return "LB_ERR_UNSUPPORTED";
     case LB_ERR_CUDA: return "LB_ERR_CUDA";
+    case LB_ERR_NOT_STARTED: return "LB_ERR_NOT_STARTED";
+    case LB_ERR_FOREIGN_OUTPUT: return "LB_ERR_FOREIGN_OUTPUT";
+    case LB_ERR_UPDATE_PENDING: return "LB_ERR_UPDATE_PENDING";
     }
     return "LB_ERR_UNKNOWN";
 }

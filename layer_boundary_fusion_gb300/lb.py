@@ -21,6 +21,9 @@ LB_ERR_INVALID_ARGUMENT = 1
 LB_ERR_MISALIGNED = 2
 LB_ERR_UNSUPPORTED = 3
 LB_ERR_CUDA = 4
+LB_ERR_NOT_STARTED = 5
+LB_ERR_FOREIGN_OUTPUT = 6
+LB_ERR_UPDATE_PENDING = 7
 LB_MAX_K = 16
 LB_MAX_TOPK = 16
 LB_MAX_SETS = 64
@@ -32,9 +35,19 @@ LB_DEVICE_ERR_TIMEOUT = 1
 LB_DEVICE_ERR_LAUNCH = 2
 LB_OPT_GEMMA_WEIGHT = 1
 
+LB_RESIDUAL_INITIAL = 0
+LB_RESIDUAL_WRITTEN = 1
+LB_RESIDUAL_PENDING = 2
+LB_CONTRIB_PARTIALS = 0
+LB_CONTRIB_MOE = 1
+
 EXPORTED = ("lb_status_string", "lb_last_cuda_error", "lb_version", "lb_launch_plan",
             "lb_device_error", "lb_fold_norm", "lb_fold_norm_fp8",
-            "lb_moe_finalize_fold_norm", "lb_slice_fold_norm", "lb_slice_fold_norm_v")
+            "lb_moe_finalize_fold_norm", "lb_slice_fold_norm", "lb_slice_fold_norm_v",
+            "lb_residual_init", "lb_residual_start", "lb_residual_leave",
+            "lb_residual_leave_moe", "lb_residual_prepare", "lb_residual_complete_output",
+            "lb_residual_fold", "lb_residual_add_to_output", "lb_residual_written",
+            "lb_residual_take_output", "lb_residual_norm")
 
 
 class Plan(ctypes.Structure):
@@ -51,6 +64,18 @@ class Plan(ctypes.Structure):
 class Options(ctypes.Structure):
     """lb_options: optional behaviour of a call."""
     _fields_ = [("flags", ctypes.c_uint), ("residual_snapshot", ctypes.c_void_p)]
+
+
+class ResidualStream(ctypes.Structure):
+    """lb_residual_stream (include/lb_residual.h): the host-side residual stream.  It
+    holds raw device pointers: keep the tensors it refers to alive while it does."""
+    _fields_ = [("magic", ctypes.c_uint32), ("started", ctypes.c_int),
+                ("state", ctypes.c_int), ("has_residual", ctypes.c_int),
+                ("serial", ctypes.c_uint64), ("residual", ctypes.c_void_p),
+                ("T", ctypes.c_int64), ("H", ctypes.c_int64), ("kind", ctypes.c_int),
+                ("K", ctypes.c_int), ("partials", ctypes.c_void_p * LB_MAX_K),
+                ("expert_out", ctypes.c_void_p), ("n_expert_rows", ctypes.c_int64),
+                ("idx", ctypes.c_void_p), ("w", ctypes.c_void_p), ("topk", ctypes.c_int)]
 
 
 class LibraryMissing(RuntimeError):
@@ -112,6 +137,24 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                                          _int, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _f32, op,
                                          _vp]
     lib.lb_slice_fold_norm_v.restype = _int
+    rs = ctypes.POINTER(ResidualStream)
+    out = ctypes.POINTER(ctypes.c_uint64)
+    u64 = ctypes.c_uint64
+    for name, args in (
+            ("lb_residual_init", [rs, _vp, _i64, _i64]),
+            ("lb_residual_start", [rs, out]),
+            ("lb_residual_leave", [rs, u64, ctypes.POINTER(_vp), _int, out]),
+            ("lb_residual_leave_moe", [rs, u64, _vp, _i64, _vp, _vp, _int, out]),
+            ("lb_residual_prepare", [rs, u64, _vp, _vp, _vp, _vp, _f32, op, _vp, out]),
+            ("lb_residual_complete_output", [rs, u64, _vp, _vp, out]),
+            ("lb_residual_fold", [rs, u64, _vp, out]),
+            ("lb_residual_add_to_output", [rs, u64, _vp, _vp, out]),
+            ("lb_residual_written", [rs, u64, _vp, out]),
+            ("lb_residual_take_output", [rs, u64, ctypes.POINTER(_vp)]),
+            ("lb_residual_norm", [rs, u64, _vp, _vp, _vp, _vp, _f32, op, _vp])):
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = _int
     _lib = lib
     return lib
 
@@ -255,3 +298,82 @@ def lb_slice_fold_norm_v(partials, T_pad, set_, set_offsets, set_counts, residua
                                     _ptr(y_out), _ptr(q_out), _ptr(scale_out), H, eps,
                                     _options(gemma, residual_snapshot), s),
            "lb_slice_fold_norm_v")
+
+
+# --------------------------------------------------------------------------------------
+# Residual stream (include/lb_residual.h).  Each function that hands on an output
+# returns its handle (an int); pass it to the next call.
+# --------------------------------------------------------------------------------------
+
+def _handle(func: str, call) -> int:
+    h = ctypes.c_uint64(0)
+    _check(call(ctypes.byref(h)), func)
+    return h.value
+
+
+def lb_residual_init(s: ResidualStream, residual, T, H) -> None:
+    _check(load().lb_residual_init(ctypes.byref(s), _ptr(residual), T, H), "lb_residual_init")
+
+
+def lb_residual_start(s: ResidualStream) -> int:
+    return _handle("lb_residual_start", lambda o: load().lb_residual_start(ctypes.byref(s), o))
+
+
+def lb_residual_leave(s: ResidualStream, h: int, partials) -> int:
+    partials = list(partials)
+    arr = _ptr_array(partials)
+    return _handle("lb_residual_leave", lambda o: load().lb_residual_leave(
+        ctypes.byref(s), h, arr, len(partials), o))
+
+
+def lb_residual_leave_moe(s: ResidualStream, h: int, expert_out, n_expert_rows, idx, w,
+                          topk) -> int:
+    return _handle("lb_residual_leave_moe", lambda o: load().lb_residual_leave_moe(
+        ctypes.byref(s), h, _ptr(expert_out), n_expert_rows, _ptr(idx), _ptr(w), topk, o))
+
+
+def lb_residual_prepare(s: ResidualStream, h: int, gamma, y_out, q_out, scale_out, eps,
+                        stream=None, *, gemma=False, residual_snapshot=None) -> int:
+    st = _stream(stream, gamma, y_out, q_out)
+    return _handle("lb_residual_prepare", lambda o: load().lb_residual_prepare(
+        ctypes.byref(s), h, _ptr(gamma), _ptr(y_out), _ptr(q_out), _ptr(scale_out), eps,
+        _options(gemma, residual_snapshot), st, o))
+
+
+def lb_residual_complete_output(s: ResidualStream, h: int, sum_out, stream=None) -> int:
+    st = _stream(stream, sum_out)
+    return _handle("lb_residual_complete_output", lambda o: load().lb_residual_complete_output(
+        ctypes.byref(s), h, _ptr(sum_out), st, o))
+
+
+def lb_residual_fold(s: ResidualStream, h: int, stream=None) -> int:
+    st = _stream(stream)
+    return _handle("lb_residual_fold",
+                   lambda o: load().lb_residual_fold(ctypes.byref(s), h, st, o))
+
+
+def lb_residual_add_to_output(s: ResidualStream, h: int, extra, stream=None) -> int:
+    st = _stream(stream, extra)
+    return _handle("lb_residual_add_to_output", lambda o: load().lb_residual_add_to_output(
+        ctypes.byref(s), h, _ptr(extra), st, o))
+
+
+def lb_residual_written(s: ResidualStream, h: int, hidden) -> int:
+    return _handle("lb_residual_written", lambda o: load().lb_residual_written(
+        ctypes.byref(s), h, _ptr(hidden), o))
+
+
+def lb_residual_take_output(s: ResidualStream, h: int) -> int:
+    """Release the stream; returns the residual buffer's device address."""
+    p = ctypes.c_void_p(0)
+    _check(load().lb_residual_take_output(ctypes.byref(s), h, ctypes.byref(p)),
+           "lb_residual_take_output")
+    return p.value or 0
+
+
+def lb_residual_norm(s: ResidualStream, h: int, gamma, y_out, q_out, scale_out, eps,
+                     stream=None, *, gemma=False, residual_snapshot=None) -> None:
+    st = _stream(stream, gamma, y_out, q_out)
+    _check(load().lb_residual_norm(ctypes.byref(s), h, _ptr(gamma), _ptr(y_out), _ptr(q_out),
+                                   _ptr(scale_out), eps, _options(gemma, residual_snapshot),
+                                   st), "lb_residual_norm")

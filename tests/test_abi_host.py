@@ -6,6 +6,7 @@ No kernel runs here.  The argument-validation cases use fake device addresses, s
 they execute in a child process that sees no GPU at all: a case that wrongly passed
 validation would get a CUDA "no device" error, never a launch on a bad address.
 """
+import glob
 import json
 import os
 import re
@@ -25,9 +26,11 @@ def lib():
 
 
 def declared_functions():
-    text = open(os.path.join(ROOT, "include", "lb.h")).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(lb_[a-z0-9_]+)\s*\(", text)))
+    names = set()
+    for h in sorted(glob.glob(os.path.join(ROOT, "include", "*.h"))):
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"\b(lb_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declares_the_four_boundary_calls():
@@ -52,6 +55,9 @@ def test_library_exports_every_declared_symbol(lib):
 def test_status_strings_and_version(lib):
     assert lib.lb_status_string(0) == "LB_OK"
     assert lib.lb_status_string(4) == "LB_ERR_CUDA"
+    assert lib.lb_status_string(5) == "LB_ERR_NOT_STARTED"
+    assert lib.lb_status_string(6) == "LB_ERR_FOREIGN_OUTPUT"
+    assert lib.lb_status_string(7) == "LB_ERR_UPDATE_PENDING"
     assert lib.lb_version() >= 100
 
 

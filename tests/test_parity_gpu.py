@@ -609,3 +609,69 @@ def test_unfused_two_call_path_matches_the_oracle(lb):
     s_got = gpu_fold(lb, w.partials, None, w.gamma, w.eps, want_y=False)["residual_out"]
     assert_bits_equal(s_got, s_want, "unfused sum")
     check_fold(gpu_fold(lb, [s_got], w.residual, w.gamma, w.eps), want, "unfused add+norm")
+
+
+@pytest.mark.parametrize("T", [40, 300])           # row kernel, stream kernel
+def test_residual_stream_through_a_layer_stack(lb, T):
+    """A layer stack driven through the residual stream (lb_residual.h): enter, a
+    completed and extended contribution with an FP8 read, fold then a plain read, and a
+    MoE handoff consumed by a Gemma final norm.  Each read and the residual after each
+    step match the oracle evaluating the same sequence of boundary operations."""
+    H, eps = 1024, 1e-6
+    fw = wl.fold_workload("stack", 4, T, H, seed=98)
+    mw = wl.moe_workload("stack_moe", T, H, 16, 4, seed=99)
+    E0, P0, P1, X = fw.partials
+    P2 = fw.residual
+    gamma = fw.gamma
+    R = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    buf = torch.empty_like(R)
+    y1, y3, y4 = (torch.empty_like(R) for _ in range(3))
+    q = torch.empty((T, H), dtype=torch.uint8, device="cuda")
+    sc = torch.empty((T,), dtype=torch.float32, device="cuda")
+    G = torch.from_numpy(gamma).cuda()
+    d = {k: dev_bits(v) for k, v in (("E0", E0), ("P0", P0), ("P1", P1), ("X", X), ("P2", P2),
+                                     ("EX", mw.expert_out))}
+    I = torch.from_numpy(mw.idx).cuda()
+    Wt = torch.from_numpy(mw.w).cuda()
+    s = lb.ResidualStream()
+    lb.lb_residual_init(s, R, T, H)
+    h = lb.lb_residual_start(s)
+    # enter: the embedding's contribution becomes the residual, then the first read
+    h = lb.lb_residual_leave(s, h, [d["E0"]])
+    h = lb.lb_residual_prepare(s, h, G, y1, None, None, eps)
+    torch.cuda.synchronize()
+    r1 = host_bits(R)
+    want1 = oracle.fold_norm([E0], None, gamma, eps)
+    check_fold({"residual_out": r1, "y": host_bits(y1)}, want1, "enter")
+    # an owed sum completed into a buffer, an extra contribution, then the FP8 read
+    h = lb.lb_residual_leave(s, h, [d["P0"], d["P1"]])
+    h = lb.lb_residual_complete_output(s, h, buf)
+    h = lb.lb_residual_add_to_output(s, h, d["X"])
+    h = lb.lb_residual_prepare(s, h, G, None, q, sc, eps)
+    torch.cuda.synchronize()
+    s_want = oracle.fold_norm([P0, P1], None, None, eps, want_y=False)["residual_out"]
+    assert_bits_equal(host_bits(buf), s_want, "complete_output")
+    want2 = oracle.fold_norm([s_want, X], r1, gamma, eps, want_y=False, want_fp8=True)
+    r2 = host_bits(R)
+    check_fold({"residual_out": r2, "q": q.cpu().numpy(), "scale": sc.cpu().numpy()}, want2,
+               "add_to_output + fp8 read")
+    # fold, then a read of the written stream
+    h = lb.lb_residual_leave(s, h, [d["P2"]])
+    h = lb.lb_residual_fold(s, h)
+    h = lb.lb_residual_prepare(s, h, G, y3, None, None, eps)
+    torch.cuda.synchronize()
+    r3_want = oracle.fold_norm([P2], r2, None, eps, want_y=False)["residual_out"]
+    r3 = host_bits(R)
+    assert_bits_equal(r3, r3_want, "fold")
+    check_fold({"y": host_bits(y3)}, oracle.fold_norm([], r3_want, gamma, eps), "read")
+    # a MoE finalize handoff consumed by a Gemma final norm, which releases the stream
+    h = lb.lb_residual_leave_moe(s, h, d["EX"], mw.expert_out.shape[0], I, Wt, mw.topk)
+    lb.lb_residual_norm(s, h, G, y4, None, None, eps, gemma=True)
+    torch.cuda.synchronize()
+    want4 = oracle.moe_finalize_fold_norm(mw.expert_out, mw.idx, mw.w, r3_want, gamma, eps,
+                                          gemma=True)
+    check_fold({"residual_out": host_bits(R), "y": host_bits(y4)}, want4, "final norm")
+    assert s.started == 0
+    with pytest.raises(lb.LBError) as e:
+        lb.lb_residual_take_output(s, h + 1)
+    assert e.value.status == lb.LB_ERR_NOT_STARTED
