@@ -118,8 +118,9 @@ typedef struct {
  * GPU with `num_sms` SMs and `smem_per_block` bytes of opt-in shared memory per CTA.
  * Host-only, pure.  Calls with at least one row per SM stream through the
  * persistent TMA kernel when a double-buffered stage fits; smaller calls use the
- * row kernel, splitting each row over a cluster when the rows alone cannot fill the
- * GPU.  Returns LB_ERR_UNSUPPORTED for an H that no launch covers.
+ * row kernel, one CTA per row, splitting a row over a cluster only when it is longer
+ * than one CTA holds (16384 elements).  Returns LB_ERR_UNSUPPORTED for an H that no
+ * launch covers.
  */
 lb_status lb_launch_plan(int64_t rows, int64_t H, int n_inputs, int num_sms,
                          int smem_per_block, lb_plan *plan);

@@ -19,6 +19,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "liblb.so")
+# Test-only variant (tests of the bounded waits): the same sources with LB_TEST_HOOKS.
+TEST_LIB = os.path.join(PKG, "liblb_test.so")
+TEST_BUILD_DIR = os.path.join(PKG, "_build_test")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
@@ -41,22 +44,28 @@ def _inputs():
         os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h")) + [__file__]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False,
+          test_hooks: bool = False) -> str:
+    """Build liblb.so (or, with test_hooks, the test-only liblb_test.so); returns its
+    path."""
+    lib, build_dir = (TEST_LIB, TEST_BUILD_DIR) if test_hooks else (LIB, BUILD_DIR)
+    if not force and up_to_date(lib):
+        return lib
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_verbose else []
+    if test_hooks:
+        extra += ["-DLB_TEST_HOOKS"]
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src) + ".o")
         cmd = [cc, *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
         if verbose:
             print(" ".join(cmd), file=sys.stderr)
@@ -69,15 +78,15 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
 
     with concurrent.futures.ThreadPoolExecutor(max_workers=len(sources())) as ex:
         objs = list(ex.map(compile_one, sources()))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     if verbose:
         print(" ".join(cmd), file=sys.stderr)
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
@@ -85,6 +94,8 @@ if __name__ == "__main__":
     ap.add_argument("--force", action="store_true")
     ap.add_argument("--ptxas-verbose", action="store_true")
     ap.add_argument("-v", "--verbose", action="store_true")
+    ap.add_argument("--test-hooks", action="store_true",
+                    help="build the test-only liblb_test.so instead")
     a = ap.parse_args()
     print(build(force=a.force or a.ptxas_verbose, verbose=a.verbose,
-                ptxas_verbose=a.ptxas_verbose))
+                ptxas_verbose=a.ptxas_verbose, test_hooks=a.test_hooks))

@@ -112,6 +112,11 @@ int device_info(DeviceInfo *out) {
     return 0;
 }
 
+#ifdef LB_TEST_HOOKS
+// Test builds only: the row whose copies the next stream-kernel launches withhold.
+static int64_t g_test_withhold_row = -1;
+#endif
+
 lb_status launch(const lb::Params &p, lb::Mode mode, bool fp8, int n_inputs,
                  cudaStream_t stream) {
     DeviceInfo d;
@@ -122,6 +127,9 @@ lb_status launch(const lb::Params &p, lb::Mode mode, bool fp8, int n_inputs,
     }
     lb::Params q = p;
     q.inv_H = 1.0f / static_cast<float>(p.H);
+#ifdef LB_TEST_HOOKS
+    q.test_withhold_row = g_test_withhold_row;
+#endif
     cudaError_t e;
     lb::StreamShape ss;
     if (lb::use_stream_kernel(p.rows, d.sms) &&
@@ -280,13 +288,9 @@ lb_status check_sets(const int32_t *set_offsets, const int32_t *set_counts, int 
 namespace lb {
 
 bool use_stream_kernel(int64_t rows, int num_sms) {
-    // Enough rows for one persistent CTA per SM; fewer rows go to the row kernel,
-    // which splits each row over a cluster to fill the GPU.
-#ifdef LB_STREAM_MIN_ROWS
-    return rows >= LB_STREAM_MIN_ROWS;
-#else
+    // Enough rows for one persistent CTA per SM; fewer rows go to the row kernel (one
+    // CTA per row; a cluster only for rows longer than one CTA holds).
     return rows >= num_sms;
-#endif
 }
 
 bool choose_stream_shape(int64_t rows, int64_t H, int n_inputs, int num_sms,
@@ -324,14 +328,6 @@ bool choose_stream_shape(int64_t rows, int64_t H, int n_inputs, int num_sms,
     ns -= ns % groups;
     const int64_t ctas = static_cast<int64_t>(num_sms) * LB_STREAM_CTAS_PER_SM;
     int64_t grid = rows < ctas ? rows : ctas;
-#ifdef LB_STREAM_BALANCED
-    // largest grid <= ctas that divides the rows evenly, if it keeps >= 3/4 of the SMs
-    for (int64_t g = grid; g * 4 >= ctas * 3; --g)
-        if (rows % g == 0) {
-            grid = g;
-            break;
-        }
-#endif
     out->grid = static_cast<int>(grid);
     out->groups = static_cast<int>(groups);
     out->consumer_warps = ncw;
@@ -353,10 +349,6 @@ bool choose_shape(int64_t rows, int64_t H, int num_sms, Shape *out) {
     // Long rows: at most 512 threads x 4 vectors per CTA, else a cluster splits them.
     while (cs < 8 && (nvec + cs - 1) / cs > 2048)
         cs *= 2;
-#ifdef LB_ROW_FORCE_CLUSTER
-    if (nvec % LB_ROW_FORCE_CLUSTER == 0)
-        cs = LB_ROW_FORCE_CLUSTER;
-#endif
     const int64_t vpc = (nvec + cs - 1) / cs;
     if (vpc > 2048)
         return false;
@@ -390,6 +382,12 @@ const char *lb_status_string(lb_status status) {
 int lb_last_cuda_error(void) { return g_last_cuda_error; }
 
 int lb_version(void) { return 100; }
+
+#ifdef LB_TEST_HOOKS
+// Test builds only (not declared in the public headers): make the stream kernel post a
+// row's bytes without issuing its copies (-1: none), to exercise the bounded waits.
+void lb_test_withhold_row(int64_t row) { g_test_withhold_row = row; }
+#endif
 
 lb_status lb_launch_plan(int64_t rows, int64_t H, int n_inputs, int num_sms,
                          int smem_per_block, lb_plan *plan) {

@@ -81,6 +81,11 @@ struct Params {
     int groups;
     int consumer_warps;
     float inv_H;
+#ifdef LB_TEST_HOOKS
+    // test builds only: the stream kernel posts this row's bytes but issues none of its
+    // copies, so that the row's consumers wait until their bounded wait runs out
+    int64_t test_withhold_row;
+#endif
 };
 
 // Row kernel: one CTA (or a cluster of CTAs) per row.

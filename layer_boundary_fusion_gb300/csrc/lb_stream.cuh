@@ -367,6 +367,10 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
             }
             if (lane == 0)
                 mbar_arrive_expect_tx(full, slot_bytes * __popc(valid));
+#ifdef LB_TEST_HOOKS
+            if (row == p.test_withhold_row)
+                src = nullptr;                   // the posted bytes never arrive
+#endif
             const uint32_t dst = stage0 + static_cast<uint32_t>(s) * stage_bytes;
             for (int j = 0; j < n_slots; ++j) {
                 const void *sj = reinterpret_cast<const void *>(

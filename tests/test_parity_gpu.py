@@ -386,6 +386,10 @@ def test_specified_workloads_take_the_intended_kernels(lb):
     (4, 1000, 4096),    # stream kernel
     (16, 300, 1024),    # stream kernel at the maximum K (17 staged rows per stage)
     (1, 2, 131072),     # the largest hidden size: a row split over an 8-CTA cluster
+    (3, 151, 4096),     # one row short of the SM count: row kernel
+    (3, 153, 8),        # stream kernel, one vector per row, a ragged wave
+    (16, 160, 24),      # stream kernel, maximum K, three vectors per row
+    (2, 200, 12288),    # row kernel beyond the SM count (rows too long to stage)
 ])
 def test_shapes(lb, K, T, H):
     w = wl.fold_workload("shape", K, T, H, seed=K * 1000 + T + H)
