@@ -229,15 +229,18 @@ def kernel_name(plan, mode, fp8):
 
 
 def kernel_source_hash():
-    """Hash of the sources the kernels are compiled from (device code and its launch
-    parameters; the host-only API files are left out)."""
+    """Hash of the sources the library's kernels are compiled from (device code and its
+    launch parameters as the product build sees them: host-only API files and blocks
+    that only the test build compiles are left out)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "layer_boundary_fusion_gb300", "csrc")
     files = sorted(glob.glob(os.path.join(csrc, "*.cuh")) +
                    [os.path.join(csrc, n) for n in ("lb_fold.cu", "lb_moe.cu", "lb_internal.h")])
     for f in files:
+        text = re.sub(rb"#ifdef LB_TEST_HOOKS\n.*?#endif\n", b"", open(f, "rb").read(),
+                      flags=re.S)
         h.update(os.path.basename(f).encode())
-        h.update(open(f, "rb").read())
+        h.update(text)
     return h.hexdigest()
 
 
