@@ -230,8 +230,8 @@ def kernel_name(plan, mode, fp8):
 
 def kernel_source_hash():
     """Hash of the sources the library's kernels are compiled from (device code and its
-    launch parameters as the product build sees them: host-only API files and blocks
-    that only the test build compiles are left out)."""
+    launch parameters as the product build sees them: host-only API files, blocks that
+    only the test build compiles, comments and blank lines are left out)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "layer_boundary_fusion_gb300", "csrc")
     files = sorted(glob.glob(os.path.join(csrc, "*.cuh")) +
@@ -239,6 +239,9 @@ def kernel_source_hash():
     for f in files:
         text = re.sub(rb"#ifdef LB_TEST_HOOKS\n.*?#endif\n", b"", open(f, "rb").read(),
                       flags=re.S)
+        text = re.sub(rb"/\*.*?\*/", b"", text, flags=re.S)     # comments do not compile
+        text = re.sub(rb"//[^\n]*", b"", text)
+        text = b"\n".join(line.rstrip() for line in text.split(b"\n") if line.strip())
         h.update(os.path.basename(f).encode())
         h.update(text)
     return h.hexdigest()

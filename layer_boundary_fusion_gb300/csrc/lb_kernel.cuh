@@ -6,9 +6,10 @@
 // pass over HBM:
 //   1. issue the residual, gamma and every partial (or gathered expert-row) load of
 //      a chunk -- all of a decode boundary's K <= 8 partials -- before consuming any;
-//   2. accumulate in binary32 pairs (packed f32x2, rounding each lane like the scalar
-//      ops) in a fixed order: +0, then k or j ascending, then the residual -- the
-//      order of the definition, so residual' is bit-identical to it;
+//   2. accumulate in binary32 in a fixed order: +0, then k or j ascending, then the
+//      residual -- the order of the definition, so residual' is bit-identical to it
+//      (bf16 inputs are added by one mixed-precision add.rn.f32.bf16 each; MoE
+//      products are rounded by scalar mul.rn before a packed f32x2 add);
 //   3. store residual', and reduce sum(o^2) (and max|o*gamma| for the FP8 read) over
 //      the row in one warp-shuffle + shared-memory step;
 //   4. r = rsqrt(sum/H + eps); store y = bf16((o*r)*gamma), or the E4M3 codes and the
@@ -249,8 +250,8 @@ __global__ void __launch_bounds__(512, 1) boundary_kernel(const __grid_constant_
         }
     }
 
-    // o in binary32 pairs, summed in the definition's order (packed adds round each
-    // lane like the scalar ones)
+    // o in binary32 pairs, summed in the definition's order (mixed-precision and packed
+    // adds round each element like the scalar binary32 add)
     float2 acc[kVpt][4];
 #pragma unroll
     for (int i = 0; i < kVpt; ++i)

@@ -5,7 +5,9 @@
 //   warp 0 (producer): for each of this CTA's rows, wait until its stage is free,
 //     post the byte count on the stage's "full" mbarrier and issue one
 //     cp.async.bulk (global -> shared) per input row: the K partial rows (or the
-//     gathered expert rows of a MoE finalize) and the residual row.
+//     gathered expert rows of a MoE finalize) and the residual row.  A MoE token's
+//     expert indices and routing weights are fetched two rows ahead (cp.async) into
+//     a ring of per-row metadata blocks beside the stages.
 //   consumer groups of W warps (rows dealt to the groups in turn, so that several
 //     rows are reduced at once): wait on "full", fold the stage's rows in binary32 in
 //     the definition's order, hand the stage back ("empty" mbarrier, one arrive per
@@ -462,9 +464,10 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
         // A thread whose wait fails reads nothing from the stage and writes nothing;
         // the group learns of it at its row barrier and leaves together.
         const bool ok = mbar_wait_bounded(full0 + 8 * s, k & 1u, &abort_flag);
-        // o in binary32 pairs: acc[v][i] holds elements 2i, 2i+1 of vector v.  Packed
-        // f32x2 adds and multiplies round each lane exactly like the scalar ones, so
-        // the order of the definition -- and residual' bit for bit -- is kept.
+        // o in binary32 pairs: acc[v][i] holds elements 2i, 2i+1 of vector v.  Mixed
+        // add.rn.f32.bf16 adds, scalar mul.rn products and packed f32x2 adds all round
+        // like the scalar binary32 ops, so the order of the definition -- and residual'
+        // bit for bit -- is kept.
         float2 acc[kVpt][4];
 #pragma unroll
         for (int v = 0; v < kVpt; ++v)
