@@ -580,6 +580,36 @@ def test_host_pipeline_matches_the_oracle(lb):
         assert_fp8_close(q.numpy(), want["q"], sc.numpy(), want["scale"], f"host fp8 {call}")
 
 
+def test_host_pipeline_overlapped_steps_keep_their_own_data(lb):
+    """Five steps with different inputs and outputs run as one pipelined schedule on
+    two device buffer sets (step i+1 copies in while step i copies out): every step's
+    outputs match the oracle on that step's inputs, so no step reads or overwrites
+    another's buffers."""
+    from layer_boundary_fusion_gb300.host import HostPipeline
+    K, T, H = 2, 300, 1024
+    ws = [wl.fold_workload("host_steps", K, T, H, seed=200 + i, fp8=True) for i in range(5)]
+    gamma = torch.from_numpy(ws[0].gamma).pin_memory()
+    inputs, outputs, wants = [], [], []
+    for w in ws:
+        inputs.append(([torch.from_numpy(p.view(np.int16)).pin_memory() for p in w.partials],
+                       torch.from_numpy(w.residual.view(np.int16)).pin_memory()))
+        outputs.append((torch.full((T, H), -1, dtype=torch.int16).pin_memory(),
+                        torch.full((T, H), 0x7F, dtype=torch.uint8).pin_memory(),
+                        torch.full((T,), float("nan"), dtype=torch.float32).pin_memory()))
+        wants.append(oracle.fold_norm(w.partials, w.residual, ws[0].gamma, w.eps,
+                                      want_y=False, want_fp8=True))
+    for chunks in (1, 3):
+        pipe = HostPipeline(K, T, H, "cuda:0", chunks=chunks, depth=2)
+        for rep in range(2):                    # capture, then replay
+            pipe.run_steps(inputs, gamma, outputs, ws[0].eps)
+            torch.cuda.synchronize()
+            for i, ((ro, q, sc), want) in enumerate(zip(outputs, wants)):
+                what = f"chunks {chunks} rep {rep} step {i}"
+                assert_bits_equal(ro.numpy().view(np.uint16), want["residual_out"], what)
+                assert_fp8_close(q.numpy(), want["q"], sc.numpy(), want["scale"], what)
+                ro.fill_(-1), q.fill_(0x7F), sc.fill_(float("nan"))
+
+
 def test_non_finite_inputs_propagate_like_the_oracle(lb):
     """A NaN or an infinity in a partial makes its row's outputs non-finite where the
     definition says so; other rows are unaffected.  Compared as float values
