@@ -390,6 +390,7 @@ def test_specified_workloads_take_the_intended_kernels(lb):
     (3, 153, 8),        # stream kernel, one vector per row, a ragged wave
     (16, 160, 24),      # stream kernel, maximum K, three vectors per row
     (2, 200, 12288),    # row kernel beyond the SM count (rows too long to stage)
+    (2, 30000, 256),    # stream kernel, ~200 rows per CTA: every stage wraps many times
 ])
 def test_shapes(lb, K, T, H):
     w = wl.fold_workload("shape", K, T, H, seed=K * 1000 + T + H)
