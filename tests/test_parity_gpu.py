@@ -710,3 +710,42 @@ def test_residual_stream_through_a_layer_stack(lb, T):
     with pytest.raises(lb.LBError) as e:
         lb.lb_residual_take_output(s, h + 1)
     assert e.value.status == lb.LB_ERR_NOT_STARTED
+
+
+def test_concurrent_host_threads_and_streams(lb):
+    """Two host threads each enqueue a chain of boundaries on their own stream at the
+    same time (the library keeps no per-call state: only a cached device description and
+    the device error word).  Each thread's results match the oracle."""
+    import threading
+    cases = []
+    for i, (K, T, H) in enumerate([(4, 300, 2048), (8, 64, 4096)]):
+        w = wl.fold_workload("threads", K, T, H, seed=400 + i)
+        cases.append((w, oracle.fold_norm(w.partials, w.residual, w.gamma, w.eps)))
+    results, errors = [None, None], []
+
+    def worker(i):
+        try:
+            w, _ = cases[i]
+            st = torch.cuda.Stream()
+            P = [dev_bits(p) for p in w.partials]
+            R = dev_bits(w.residual)
+            G = torch.from_numpy(w.gamma).cuda()
+            outs = [(torch.empty_like(R), torch.empty_like(R)) for _ in range(20)]
+            torch.cuda.synchronize()
+            with torch.cuda.stream(st):
+                for ro, yo in outs:
+                    lb.lb_fold_norm(P, R, ro, G, yo, w.T, w.H, w.eps, stream=st)
+            st.synchronize()
+            results[i] = [(host_bits(ro), host_bits(yo)) for ro, yo in outs]
+        except Exception as e:       # reported by the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for (w, want), res in zip(cases, results):
+        for ro, yo in res:
+            check_fold({"residual_out": ro, "y": yo}, want, f"thread K={w.K}")
