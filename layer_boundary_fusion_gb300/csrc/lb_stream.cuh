@@ -168,6 +168,19 @@ __device__ __forceinline__ void cp_async_wait_pending(int n) {
     }
 }
 
+// Streaming stores (st.global.cs: evict-first in L2) for outputs nothing in this
+// launch reads back.
+__device__ __forceinline__ void st_stream16(void *ptr, uint4 v) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(ptr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_stream8(void *ptr, uint2 v) {
+    asm volatile("st.global.cs.v2.u32 [%0], {%1, %2};" ::"l"(ptr), "r"(v.x), "r"(v.y)
+                 : "memory");
+}
+
 // ------------------------------------------------------------------------------------
 // Row schedule shared by producer and consumers
 // ------------------------------------------------------------------------------------
@@ -519,7 +532,7 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
                 if (act[v]) {
                     const uint4 packed = pack8x2(acc[v]);
                     if (p.residual_out != nullptr)
-                        *reinterpret_cast<uint4 *>(p.residual_out + roff + col[v]) = packed;
+                        st_stream16(p.residual_out + roff + col[v], packed);
                     if (p.snapshot != nullptr)
                         *reinterpret_cast<uint4 *>(p.snapshot + roff + col[v]) = packed;
                 }
@@ -615,7 +628,7 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
                                         (cvt_e4m3x2(q[1].x, q[1].y) << 16);
                     const uint32_t hi = cvt_e4m3x2(q[2].x, q[2].y) |
                                         (cvt_e4m3x2(q[3].x, q[3].y) << 16);
-                    *reinterpret_cast<uint2 *>(p.q_out + roff + col[v]) = make_uint2(lo, hi);
+                    st_stream8(p.q_out + roff + col[v], make_uint2(lo, hi));
                 }
         } else {
 #pragma unroll
