@@ -42,8 +42,10 @@ class HostPipeline:
     the host; results residual' [T, H] (int16 bits), codes [T, H] uint8 and scales
     [T] float32 on the host.  `chunks` row blocks per step (rows must divide evenly),
     `depth` device buffer sets (consecutive steps overlap when depth >= 2).  One CUDA
-    graph is kept per distinct sequence of host buffers.
+    graph is kept per distinct sequence of host buffers (the MAX_GRAPHS most recent).
     """
+
+    MAX_GRAPHS = 8                        # captured schedules kept (oldest dropped first)
 
     def __init__(self, K: int, T: int, H: int, device, chunks: int = 1, depth: int = 2):
         if T % chunks:
@@ -56,7 +58,7 @@ class HostPipeline:
         self.s_run = torch.cuda.Stream(self.dev)
         self.s_out = torch.cuda.Stream(self.dev)
         self.sets = [_DeviceSet(K, T, H, self.dev) for _ in range(depth)]
-        self.graphs = {}
+        self.graphs = {}                  # host-buffer sequence -> graph, oldest first
 
     def _schedule(self, steps, inputs, gamma_host, outputs, eps, origin):
         """Enqueue `steps` steps: fork from `origin`, pipelined copy-in / kernel /
@@ -128,6 +130,8 @@ class HostPipeline:
                 self._schedule(len(inputs), lambda i: inputs[i], gamma_host,
                                lambda i: outputs[i], eps, cap)
             origin.wait_stream(cap)
+            if len(self.graphs) >= self.MAX_GRAPHS:
+                self.graphs.pop(next(iter(self.graphs)))
             self.graphs[key] = graph
         with torch.cuda.stream(origin):
             graph.replay()
