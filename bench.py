@@ -229,13 +229,13 @@ def kernel_name(plan, mode, fp8):
 
 
 def kernel_source_hash():
-    """Hash of the sources the library's kernels are compiled from (device code and its
-    launch parameters as the product build sees them: host-only API files, blocks that
-    only the test build compiles, comments and blank lines are left out)."""
+    """Hash of the files that define the library's kernels (their device code, the
+    parameter block and the launch-shape constants) as the product build sees them:
+    host-side launch and API files, blocks that only the test build compiles, comments
+    and blank lines are left out."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "layer_boundary_fusion_gb300", "csrc")
-    files = sorted(glob.glob(os.path.join(csrc, "*.cuh")) +
-                   [os.path.join(csrc, n) for n in ("lb_fold.cu", "lb_moe.cu", "lb_internal.h")])
+    files = [os.path.join(csrc, n) for n in ("lb_internal.h", "lb_kernel.cuh", "lb_stream.cuh")]
     for f in files:
         text = re.sub(rb"#ifdef LB_TEST_HOOKS\n.*?#endif\n", b"", open(f, "rb").read(),
                       flags=re.S)

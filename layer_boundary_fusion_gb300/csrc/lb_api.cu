@@ -85,6 +85,7 @@ lb_status check_tensor(const void *p) {
 struct DeviceInfo {
     int sms;
     int smem_optin;
+    int device;
 };
 
 int device_info(DeviceInfo *out) {
@@ -99,6 +100,7 @@ int device_info(DeviceInfo *out) {
         return 0;
     }
     DeviceInfo d{};
+    d.device = dev;
     e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess)
         e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
@@ -134,6 +136,8 @@ lb_status launch(const lb::Params &p, lb::Mode mode, bool fp8, int n_inputs,
     lb::StreamShape ss;
     if (lb::use_stream_kernel(p.rows, d.sms) &&
         lb::choose_stream_shape(p.rows, p.H, n_inputs, d.sms, d.smem_optin, &ss)) {
+        ss.device = d.device;
+        ss.smem_optin = d.smem_optin;
         q.stages = ss.stages;
         q.groups = ss.groups;
         q.consumer_warps = ss.consumer_warps;

@@ -1,6 +1,6 @@
 // Fold-mode kernels: K partial buffers (lb_fold_norm, lb_fold_norm_fp8 and the row
 // slice of a ragged batch, lb_slice_fold_norm), row and stream variants.
-#include "lb_stream.cuh"
+#include "lb_launch.cuh"
 
 namespace lb {
 

@@ -103,6 +103,8 @@ struct StreamShape {
     int vpt;             // vectors per consumer thread (1, 2 or 4)
     int stages;          // 2..8
     int smem_bytes;      // dynamic shared memory per CTA
+    int device;          // launch: the current device (-1 if unknown)
+    int smem_optin;      // launch: the device's opt-in shared memory per CTA
 };
 
 // Pure host functions choosing the launch.  n_inputs = input rows read per output row.

@@ -451,47 +451,4 @@ __global__ void __launch_bounds__(512, 1) boundary_kernel(const __grid_constant_
         cluster_wait();                            // keep our share alive for the peers
 }
 
-// ------------------------------------------------------------------------------------
-// Host-side launch
-// ------------------------------------------------------------------------------------
-
-template <int kMode, bool kFp8, int kVpt>
-cudaError_t launch_variant(const Params &p, const Shape &s, cudaStream_t stream) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(p.rows * s.ctas_per_row), 1, 1);
-    cfg.blockDim = dim3(static_cast<unsigned>(s.threads), 1, 1);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (s.ctas_per_row > 1) {
-        attr[1].id = cudaLaunchAttributeClusterDimension;
-        attr[1].val.clusterDim.x = static_cast<unsigned>(s.ctas_per_row);
-        attr[1].val.clusterDim.y = 1;
-        attr[1].val.clusterDim.z = 1;
-        cfg.numAttrs = 2;
-    }
-    return cudaLaunchKernelEx(&cfg, boundary_kernel<kMode, kFp8, kVpt>, p);
-}
-
-template <int kMode>
-cudaError_t launch_mode(const Params &p, const Shape &s, bool fp8, cudaStream_t stream) {
-    switch (s.vpt) {
-    case 1:
-        return fp8 ? launch_variant<kMode, true, 1>(p, s, stream)
-                   : launch_variant<kMode, false, 1>(p, s, stream);
-    case 2:
-        return fp8 ? launch_variant<kMode, true, 2>(p, s, stream)
-                   : launch_variant<kMode, false, 2>(p, s, stream);
-    case 4:
-        return fp8 ? launch_variant<kMode, true, 4>(p, s, stream)
-                   : launch_variant<kMode, false, 4>(p, s, stream);
-    default:
-        return cudaErrorInvalidConfiguration;
-    }
-}
-
 }  // namespace lb

@@ -1,6 +1,6 @@
 // MoE-mode kernels: the deferred finalize over gathered expert rows
 // (lb_moe_finalize_fold_norm), row and stream variants.
-#include "lb_stream.cuh"
+#include "lb_launch.cuh"
 
 namespace lb {
 

@@ -640,48 +640,4 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
     }
 }
 
-// ------------------------------------------------------------------------------------
-// Host-side launch
-// ------------------------------------------------------------------------------------
-
-template <int kMode, bool kFp8, int kVpt>
-cudaError_t launch_stream_variant(const Params &p, const StreamShape &s, cudaStream_t stream) {
-    auto kern = stream_kernel<kMode, kFp8, kVpt>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         s.smem_bytes);
-    if (e != cudaSuccess)
-        return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(s.grid), 1, 1);
-    cfg.blockDim = dim3(static_cast<unsigned>(32 * (1 + s.groups * s.consumer_warps)), 1, 1);
-    if (cfg.blockDim.x > static_cast<unsigned>(StreamThreads<kVpt>::value))
-        return cudaErrorInvalidConfiguration;
-    cfg.dynamicSmemBytes = static_cast<size_t>(s.smem_bytes);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, p);
-}
-
-template <int kMode>
-cudaError_t launch_stream_mode(const Params &p, const StreamShape &s, bool fp8,
-                               cudaStream_t stream) {
-    switch (s.vpt) {
-    case 1:
-        return fp8 ? launch_stream_variant<kMode, true, 1>(p, s, stream)
-                   : launch_stream_variant<kMode, false, 1>(p, s, stream);
-    case 2:
-        return fp8 ? launch_stream_variant<kMode, true, 2>(p, s, stream)
-                   : launch_stream_variant<kMode, false, 2>(p, s, stream);
-    case 4:
-        return fp8 ? launch_stream_variant<kMode, true, 4>(p, s, stream)
-                   : launch_stream_variant<kMode, false, 4>(p, s, stream);
-    default:
-        return cudaErrorInvalidConfiguration;
-    }
-}
-
 }  // namespace lb
