@@ -139,6 +139,42 @@ __device__ __forceinline__ float warp_max(float v) {
     return r;
 }
 
+// E4M3 codes of 8 read values (element 2e in x[e].x, 2e+1 in x[e].y), packed low byte
+// first.  Normally x * (448 / amax); when that reciprocal is not a finite positive
+// binary32 (a read so small that its scale amax / 448 is subnormal) the codes come from
+// x / scale, the definition's own division, out of line since ordinary data never
+// takes that path.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi);
+
+static __device__ __noinline__ uint2 e4m3x8_divided(float2 x0, float2 x1, float2 x2, float2 x3,
+                                                    float amax) {
+    const float scale = amax / 448.0f;
+    return make_uint2(cvt_e4m3x2(__fdiv_rn(x0.x, scale), __fdiv_rn(x0.y, scale)) |
+                          (cvt_e4m3x2(__fdiv_rn(x1.x, scale), __fdiv_rn(x1.y, scale)) << 16),
+                      cvt_e4m3x2(__fdiv_rn(x2.x, scale), __fdiv_rn(x2.y, scale)) |
+                          (cvt_e4m3x2(__fdiv_rn(x3.x, scale), __fdiv_rn(x3.y, scale)) << 16));
+}
+
+__device__ __forceinline__ uint2 e4m3x8(const float2 x[4], float inv, float amax,
+                                        bool direct) {
+    if (direct)
+        return e4m3x8_divided(x[0], x[1], x[2], x[3], amax);
+    float2 q[4];
+    const float2 inv2 = make_float2(inv, inv);
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+        q[e] = __fmul2_rn(x[e], inv2);
+    return make_uint2(cvt_e4m3x2(q[0].x, q[0].y) | (cvt_e4m3x2(q[1].x, q[1].y) << 16),
+                      cvt_e4m3x2(q[2].x, q[2].y) | (cvt_e4m3x2(q[3].x, q[3].y) << 16));
+}
+
+// 448 / amax, and whether it must be replaced by dividing by the scale.
+__device__ __forceinline__ float fp8_inverse(float amax, bool *direct) {
+    const float inv = __fdividef(448.0f, amax);
+    *direct = !(inv > 0.0f && inv <= 3.40282347e38f);
+    return inv;
+}
+
 // Two floats -> two E4M3 codes (round to nearest even, saturate to +-448); the first
 // argument lands in the low byte.  cvt puts its first source in the high half.
 __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
@@ -425,25 +461,18 @@ __global__ void __launch_bounds__(512, 1) boundary_kernel(const __grid_constant_
                 *reinterpret_cast<uint4 *>(p.y_out + row * H + col[i]) = pack8x2(acc[i]);
     }
     if (kFp8) {
-        // FP8 read: scale = amax / 448, q = E4M3(yf * 448 / amax); an all-zero row gets
-        // scale 0 and codes 0x00.
+        // FP8 read: scale = amax / 448, q = E4M3(yf * 448 / amax) (yf / scale for a
+        // subnormal scale); an all-zero row gets scale 0 and codes 0x00.
         const float amax = __fmul_rn(r, mg);
         if (threadIdx.x == 0 && crank == 0)
             p.scale_out[row] = amax / 448.0f;
-        const float inv = amax > 0.0f ? __fdividef(448.0f, amax) : 0.0f;
-        const float2 inv2 = make_float2(inv, inv);
+        bool direct = false;
+        const float inv = amax > 0.0f ? fp8_inverse(amax, &direct) : 0.0f;
 #pragma unroll
         for (int i = 0; i < kVpt; ++i)
             if (act[i]) {
-                uint2 out = make_uint2(0u, 0u);
-                if (amax > 0.0f) {
-                    float2 q[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        q[e] = __fmul2_rn(acc[i][e], inv2);
-                    out.x = cvt_e4m3x2(q[0].x, q[0].y) | (cvt_e4m3x2(q[1].x, q[1].y) << 16);
-                    out.y = cvt_e4m3x2(q[2].x, q[2].y) | (cvt_e4m3x2(q[3].x, q[3].y) << 16);
-                }
+                const uint2 out =
+                    amax > 0.0f ? e4m3x8(acc[i], inv, amax, direct) : make_uint2(0u, 0u);
                 *reinterpret_cast<uint2 *>(p.q_out + row * H + col[i]) = out;
             }
     }

@@ -609,27 +609,18 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
             continue;
         }
 
-        // FP8 read: scale = amax / 448, q = E4M3(yf * 448 / amax); an all-zero row
-        // (amax = 0) gets scale 0 and codes 0x00.
+        // FP8 read: scale = amax / 448, q = E4M3(yf * 448 / amax) (yf / scale for a
+        // subnormal scale); an all-zero row (amax = 0) gets scale 0 and codes 0x00.
         const float amax = __fmul_rn(r, mg);
         if (ct == 0)
             p.scale_out[row] = amax / 448.0f;
         if (amax > 0.0f) {
-            const float inv = __fdividef(448.0f, amax);
-            const float2 inv2 = make_float2(inv, inv);
+            bool direct;
+            const float inv = fp8_inverse(amax, &direct);
 #pragma unroll
             for (int v = 0; v < kVpt; ++v)
-                if (act[v]) {
-                    float2 q[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        q[e] = __fmul2_rn(acc[v][e], inv2);
-                    const uint32_t lo = cvt_e4m3x2(q[0].x, q[0].y) |
-                                        (cvt_e4m3x2(q[1].x, q[1].y) << 16);
-                    const uint32_t hi = cvt_e4m3x2(q[2].x, q[2].y) |
-                                        (cvt_e4m3x2(q[3].x, q[3].y) << 16);
-                    st_stream8(p.q_out + roff + col[v], make_uint2(lo, hi));
-                }
+                if (act[v])
+                    st_stream8(p.q_out + roff + col[v], e4m3x8(acc[v], inv, amax, direct));
         } else {
 #pragma unroll
             for (int v = 0; v < kVpt; ++v)

@@ -749,3 +749,23 @@ def test_concurrent_host_threads_and_streams(lb):
     for (w, want), res in zip(cases, results):
         for ro, yo in res:
             check_fold({"residual_out": ro, "y": yo}, want, f"thread K={w.K}")
+
+
+def test_fp8_read_of_near_zero_rows(lb):
+    """Rows whose read is tiny (bf16 subnormal inputs: the per-token scale is a binary32
+    subnormal, its reciprocal overflows) and rows of ordinary size side by side, on both
+    kernels: codes and scales match the oracle, which divides by the scale."""
+    for T in (100, 300):                       # row kernel, stream kernel
+        w = wl.fold_workload("tiny_rows", 2, T, 1024, seed=97)
+        P = [p.copy() for p in w.partials]
+        R = w.residual.copy()
+        rng = np.random.default_rng(5)
+        for t in range(0, T, 3):               # every third row: subnormal bf16 values
+            top = 128 if t % 2 else 3           # and every sixth the smallest of them
+            for arr in P + [R]:
+                mant = rng.integers(1, top, arr.shape[1]).astype(np.uint16)
+                sign = (rng.integers(0, 2, arr.shape[1]).astype(np.uint16) << 15)
+                arr[t] = sign | mant            # exponent 0: subnormal
+        want = oracle.fold_norm(P, R, w.gamma, w.eps, want_y=False, want_fp8=True)
+        got = gpu_fold(lb, P, R, w.gamma, w.eps, want_y=False, fp8=True)
+        check_fold(got, want, f"near-zero rows T={T}")
