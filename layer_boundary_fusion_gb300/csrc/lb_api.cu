@@ -310,6 +310,21 @@ bool choose_stream_shape(int64_t rows, int64_t H, int n_inputs, int num_sms,
     if (vpt > 4)
         return false;
     vpt = vpt <= 1 ? 1 : (vpt <= 2 ? 2 : 4);
+    // Rows of up to 2 * 32 * LB_STREAM_CONSUMER_WARPS_WIDE vectors keep two vectors per
+    // thread with wider groups (as many as fit the two-vector thread budget) rather than
+    // four vectors per thread in a single narrow group.
+    int64_t groups_cap = vpt >= 4 ? LB_STREAM_GROUPS_WIDE : LB_STREAM_GROUPS;
+    if (vpt == 4 && nvec <= 2 * 32 * LB_STREAM_CONSUMER_WARPS_WIDE) {
+        ncw = static_cast<int>((nvec + 63) / 64);
+        ncw += ncw & 1;
+        vpt = 2;
+        const int64_t budget = LB_STREAM_THREADS_2 / 32 - 1;   // consumer warps available
+        groups_cap = budget / ncw;
+        if (groups_cap < 1)
+            groups_cap = 1;
+        if (groups_cap > LB_STREAM_GROUPS)
+            groups_cap = LB_STREAM_GROUPS;
+    }
     const int64_t stage = static_cast<int64_t>(n_inputs) * H * 2;
     const int64_t reserve = 1024;              // static shared memory and mbarriers
     int64_t per_cta = LB_SMEM_PER_SM / LB_STREAM_CTAS_PER_SM - 1024;
@@ -326,7 +341,7 @@ bool choose_stream_shape(int64_t rows, int64_t H, int n_inputs, int num_sms,
     // multiple of the group count, so that every stage belongs to one group and its
     // uses are consumed in order: a parity wait on an mbarrier tells only two
     // consecutive phases apart.
-    int64_t groups = vpt >= 4 ? LB_STREAM_GROUPS_WIDE : LB_STREAM_GROUPS;
+    int64_t groups = groups_cap;
     if (groups > ns)
         groups = ns;
     ns -= ns % groups;

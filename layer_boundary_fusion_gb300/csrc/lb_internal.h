@@ -24,6 +24,13 @@
 #ifndef LB_STREAM_GROUPS_WIDE
 #define LB_STREAM_GROUPS_WIDE 1
 #endif
+// consumer warps per group when rows of up to 2 x 32 x this many vectors keep two
+// vectors per thread (hidden sizes up to 8192 at 16)
+#ifndef LB_STREAM_CONSUMER_WARPS_WIDE
+#define LB_STREAM_CONSUMER_WARPS_WIDE 16
+#endif
+// threads per CTA the two-vector stream kernel is compiled for (launch bounds)
+#define LB_STREAM_THREADS_2 (32 * (1 + LB_STREAM_GROUPS * LB_STREAM_CONSUMER_WARPS))
 #ifndef LB_STREAM_MAX_STAGES
 #define LB_STREAM_MAX_STAGES 8
 #endif

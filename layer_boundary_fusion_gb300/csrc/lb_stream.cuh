@@ -230,6 +230,10 @@ struct StreamThreads {
     static constexpr int groups = (kVpt >= 4) ? LB_STREAM_GROUPS_WIDE : LB_STREAM_GROUPS;
     static constexpr int value = 32 * (1 + groups * LB_STREAM_CONSUMER_WARPS);
 };
+// Warps of one consumer group at most (the wide-row shapes use up to 16).
+constexpr int kMaxGroupWarps = LB_STREAM_CONSUMER_WARPS > LB_STREAM_CONSUMER_WARPS_WIDE
+                                   ? LB_STREAM_CONSUMER_WARPS
+                                   : LB_STREAM_CONSUMER_WARPS_WIDE;
 constexpr int kGroupsMax =
     LB_STREAM_GROUPS > LB_STREAM_GROUPS_WIDE ? LB_STREAM_GROUPS : LB_STREAM_GROUPS_WIDE;
 
@@ -262,7 +266,7 @@ template <int kMode, bool kFp8, int kVpt>
 __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
     stream_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ __align__(16) float2 red[kGroupsMax][2][LB_STREAM_CONSUMER_WARPS];
+    __shared__ __align__(16) float2 red[kGroupsMax][2][kMaxGroupWarps];
     __shared__ int abort_flag;
 
     const int warp = threadIdx.x >> 5;

@@ -79,7 +79,8 @@ SMEM = 232448          # opt-in shared memory per CTA on GB300
     (64, 4096, 9, (0, 64, 512, 1, 1, 0, 0)),            # decode: row kernel, a CTA per row
     (1, 4096, 2, (0, 1, 512, 1, 1, 0, 0)),
     (16, 512, 3, (0, 16, 64, 1, 1, 0, 0)),              # tiny: one CTA per row
-    (4096, 8192, 5, (1, 152, 288, 4, 1, 2, 164448)),
+    (4096, 8192, 5, (1, 152, 544, 2, 1, 2, 164448)),    # one group of 16 warps
+    (4096, 6144, 2, (1, 152, 800, 2, 1, 8, 199040)),    # two groups of 12 warps
     (4096, 8192, 9, (0, 4096, 512, 2, 1, 0, 0)),        # no double-buffered stage fits
     (4096, 16384, 3, (0, 4096, 512, 4, 1, 0, 0)),
     (4096, 32768, 2, (0, 8192, 512, 4, 2, 0, 0)),
@@ -107,10 +108,13 @@ def test_launch_plan_covers_every_row_vector(lib):
                     assert p.grid == rows * p.ctas_per_row
                 else:
                     groups = p.groups
-                    assert groups == (1 if p.vectors_per_thread == 4 else min(3, p.stages))
+                    assert 1 <= groups <= min(3, p.stages) and p.threads <= 800
                     consumers = (p.threads - 32) // groups
-                    assert consumers % 32 == 0 and 32 <= consumers <= 256
+                    assert consumers * groups + 32 == p.threads
+                    assert consumers % 64 == 0 and 64 <= consumers <= 512
                     assert consumers * p.vectors_per_thread >= nvec
+                    if consumers > 256:          # wide groups keep two vectors a thread
+                        assert p.vectors_per_thread == 2
                     assert 2 <= p.stages <= 8 and p.grid == min(rows, 152)
                     # every stage belongs to one consumer group
                     assert p.stages % groups == 0

@@ -391,6 +391,9 @@ def test_specified_workloads_take_the_intended_kernels(lb):
     (16, 160, 24),      # stream kernel, maximum K, three vectors per row
     (2, 200, 12288),    # row kernel beyond the SM count (rows too long to stage)
     (2, 30000, 256),    # stream kernel, ~200 rows per CTA: every stage wraps many times
+    (4, 300, 5120),     # stream kernel, two groups of 10 warps
+    (4, 300, 6144),     # stream kernel, two groups of 12 warps
+    (3, 200, 7168),     # stream kernel, one group of 14 warps
 ])
 def test_shapes(lb, K, T, H):
     w = wl.fold_workload("shape", K, T, H, seed=K * 1000 + T + H)
