@@ -110,6 +110,7 @@ typedef struct {
     int stages;             /* stream kernel: shared-memory stages; else 0 */
     int smem_bytes;         /* stream kernel: dynamic shared memory per CTA; else 0 */
     int groups;             /* stream kernel: consumer groups (rows reduced at once) */
+    int chunks;             /* stream kernel: stages per row (column chunks); else 0 */
 } lb_plan;
 
 /*
@@ -117,10 +118,11 @@ typedef struct {
  * input rows (K partials or topk expert rows, plus one if there is a residual), on a
  * GPU with `num_sms` SMs and `smem_per_block` bytes of opt-in shared memory per CTA.
  * Host-only, pure.  Calls with at least one row per SM stream through the
- * persistent TMA kernel when a double-buffered stage fits; smaller calls use the
- * row kernel, one CTA per row, splitting a row over a cluster only when it is longer
- * than one CTA holds (16384 elements).  Returns LB_ERR_UNSUPPORTED for an H that no
- * launch covers.
+ * persistent TMA kernel when a double-buffered stage fits (a stage holds a whole row
+ * of every input, or for rows of more than 8192 elements, up to 16384, one of 2-4
+ * column chunks of it); smaller calls use the row kernel, one CTA per row, splitting
+ * a row over a cluster only when it is longer than one CTA holds (16384 elements).
+ * Returns LB_ERR_UNSUPPORTED for an H that no launch covers.
  */
 lb_status lb_launch_plan(int64_t rows, int64_t H, int n_inputs, int num_sms,
                          int smem_per_block, lb_plan *plan);

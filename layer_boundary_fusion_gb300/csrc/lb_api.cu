@@ -303,56 +303,82 @@ bool choose_stream_shape(int64_t rows, int64_t H, int n_inputs, int num_sms,
         num_sms <= 0)
         return false;
     const int64_t nvec = H / 8;
-    const int64_t maxw = LB_STREAM_CONSUMER_WARPS;
-    int ncw = static_cast<int>(nvec >= 32 * maxw ? maxw : (nvec + 31) / 32);
-    ncw += ncw & 1;                            // an even number of warps per group
-    int64_t vpt = (nvec + ncw * 32 - 1) / (ncw * 32);
-    if (vpt > 4)
-        return false;
-    vpt = vpt <= 1 ? 1 : (vpt <= 2 ? 2 : 4);
-    // Rows of up to 2 * 32 * LB_STREAM_CONSUMER_WARPS_WIDE vectors keep two vectors per
-    // thread with wider groups (as many as fit the two-vector thread budget) rather than
-    // four vectors per thread in a single narrow group.
-    int64_t groups_cap = vpt >= 4 ? LB_STREAM_GROUPS_WIDE : LB_STREAM_GROUPS;
-    if (vpt == 4 && nvec <= 2 * 32 * LB_STREAM_CONSUMER_WARPS_WIDE) {
-        ncw = static_cast<int>((nvec + 63) / 64);
-        ncw += ncw & 1;
-        vpt = 2;
-        const int64_t budget = LB_STREAM_THREADS_2 / 32 - 1;   // consumer warps available
-        groups_cap = budget / ncw;
-        if (groups_cap < 1)
-            groups_cap = 1;
-        if (groups_cap > LB_STREAM_GROUPS)
-            groups_cap = LB_STREAM_GROUPS;
-    }
-    const int64_t stage = static_cast<int64_t>(n_inputs) * H * 2;
-    const int64_t reserve = 1024;              // static shared memory and mbarriers
+    const int64_t wide = LB_STREAM_CONSUMER_WARPS_WIDE;
     int64_t per_cta = LB_SMEM_PER_SM / LB_STREAM_CTAS_PER_SM - 1024;
     if (per_cta > smem_per_block)
         per_cta = smem_per_block;
-    // per stage: its input rows, two mbarriers and two row-metadata blocks
-    const int64_t per_stage = stage + 16 + 2 * LB_STREAM_META_BYTES;
-    int64_t ns = (per_cta - reserve) / per_stage;
-    if (ns > LB_STREAM_MAX_STAGES)
-        ns = LB_STREAM_MAX_STAGES;
-    if (ns < 2)
-        return false;
-    // Row i uses stage i % ns and consumer group i % groups.  The stage count is a
+    const int64_t reserve = 1024;              // static shared memory and mbarriers
+    // Stages that fit when a stage holds `width` columns of every input row: per
+    // stage its input rows, two mbarriers and two row-metadata blocks, plus (chunked
+    // rows) the read weight of H floats once.
+    auto stages_for = [&](int64_t width, int64_t weight_bytes) {
+        const int64_t per_stage =
+            static_cast<int64_t>(n_inputs) * width * 2 + 16 + 2 * LB_STREAM_META_BYTES;
+        int64_t ns = (per_cta - reserve - weight_bytes) / per_stage;
+        return ns > LB_STREAM_MAX_STAGES ? static_cast<int64_t>(LB_STREAM_MAX_STAGES) : ns;
+    };
+    int ncw = 0;                               // warps per consumer group (even)
+    int64_t vpt = 0;                           // vectors per thread; 4 = chunked rows
+    int64_t chunks = 1;                        // stages per row
+    int64_t groups_cap = LB_STREAM_GROUPS;
+    int64_t ns = 0;
+    if (nvec < LB_STREAM_CHUNK_FROM) {
+        // Whole rows per stage.
+        if (nvec <= 2 * 32 * LB_STREAM_CONSUMER_WARPS) {
+            const int64_t maxw = LB_STREAM_CONSUMER_WARPS;
+            ncw = static_cast<int>(nvec >= 32 * maxw ? maxw : (nvec + 31) / 32);
+            ncw += ncw & 1;                    // an even number of warps per group
+            vpt = (nvec + ncw * 32 - 1) / (ncw * 32) <= 1 ? 1 : 2;
+        } else {
+            // Rows of up to 2 x 32 x `wide` vectors keep two vectors per thread with
+            // wider groups (as many as fit the two-vector thread budget).
+            ncw = static_cast<int>((nvec + 63) / 64);
+            ncw += ncw & 1;
+            vpt = 2;
+            groups_cap = (LB_STREAM_THREADS_2 / 32 - 1) / ncw;   // consumer warps left
+        }
+        ns = groups_cap >= 1 ? stages_for(H, 0) : 0;
+    }
+    if (ns < 2 && nvec < LB_STREAM_CHUNK_FROM)
+        return false;                          // many inputs: the row kernel measured faster
+    if (ns < 2) {
+        // Long rows: 2-4 column chunks of 32 x ncw vectors, one group of up to `wide`
+        // warps; chunk c holds the row's vectors [c, c + 1) x 32 x ncw and thread t
+        // keeps vector t of each.
+        ns = 0;
+        for (chunks = 2; chunks <= 4 && ns < 2; ++chunks) {
+            ncw = static_cast<int>((nvec + 32 * chunks - 1) / (32 * chunks));
+            ncw += ncw & 1;
+            if (ncw > wide)
+                continue;
+            ns = stages_for(static_cast<int64_t>(ncw) * 256, H * 4);
+        }
+        if (ns < 2)
+            return false;
+        chunks = (nvec + 32 * ncw - 1) / (32 * ncw);   // the last chunk may be short
+        vpt = 4;
+        groups_cap = 1;
+    }
+    // Row i uses stage i % ns and consumer group i % groups (chunked rows: chunk c of
+    // row i uses stage (i x chunks + c) % ns, one group).  The stage count is a
     // multiple of the group count, so that every stage belongs to one group and its
     // uses are consumed in order: a parity wait on an mbarrier tells only two
     // consecutive phases apart.
-    int64_t groups = groups_cap;
+    int64_t groups = groups_cap > LB_STREAM_GROUPS ? LB_STREAM_GROUPS : groups_cap;
     if (groups > ns)
         groups = ns;
     ns -= ns % groups;
+    const int64_t width = chunks > 1 ? static_cast<int64_t>(ncw) * 256 : H;
+    const int64_t per_stage =
+        static_cast<int64_t>(n_inputs) * width * 2 + 16 + 2 * LB_STREAM_META_BYTES;
     const int64_t ctas = static_cast<int64_t>(num_sms) * LB_STREAM_CTAS_PER_SM;
-    int64_t grid = rows < ctas ? rows : ctas;
-    out->grid = static_cast<int>(grid);
+    out->grid = static_cast<int>(rows < ctas ? rows : ctas);
     out->groups = static_cast<int>(groups);
     out->consumer_warps = ncw;
     out->vpt = static_cast<int>(vpt);
+    out->chunks = static_cast<int>(chunks);
     out->stages = static_cast<int>(ns);
-    out->smem_bytes = static_cast<int>(ns * per_stage);
+    out->smem_bytes = static_cast<int>(ns * per_stage + (chunks > 1 ? H * 4 : 0));
     return true;
 }
 
@@ -424,6 +450,7 @@ lb_status lb_launch_plan(int64_t rows, int64_t H, int n_inputs, int num_sms,
         plan->stages = ss.stages;
         plan->smem_bytes = ss.smem_bytes;
         plan->groups = ss.groups;
+        plan->chunks = ss.chunks;
         return LB_OK;
     }
     lb::Shape s;

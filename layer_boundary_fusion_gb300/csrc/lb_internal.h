@@ -20,17 +20,21 @@
 #ifndef LB_STREAM_GROUPS
 #define LB_STREAM_GROUPS 3
 #endif
-// consumer groups when each thread owns four vectors (long rows: more registers)
-#ifndef LB_STREAM_GROUPS_WIDE
-#define LB_STREAM_GROUPS_WIDE 1
-#endif
-// consumer warps per group when rows of up to 2 x 32 x this many vectors keep two
-// vectors per thread (hidden sizes up to 8192 at 16)
+// Consumer warps of one group for long rows: rows of up to 2 x 32 x this many vectors
+// keep two vectors per thread in one stage (hidden sizes up to 8192 at 16); rows of up
+// to twice that are split into column chunks of 32 x (group warps) vectors, one chunk
+// per stage, in a single group whose threads keep one vector of every chunk.
 #ifndef LB_STREAM_CONSUMER_WARPS_WIDE
 #define LB_STREAM_CONSUMER_WARPS_WIDE 16
 #endif
-// threads per CTA the two-vector stream kernel is compiled for (launch bounds)
+// Rows of at least this many 16-byte vectors are split into chunks (at most 4).
+#ifndef LB_STREAM_CHUNK_FROM
+#define LB_STREAM_CHUNK_FROM (2 * 32 * LB_STREAM_CONSUMER_WARPS_WIDE + 1)
+#endif
+// threads per CTA the stream kernel is compiled for (launch bounds): whole-row stages
+// (1 or 2 vectors per thread) and chunked rows (4 chunks per thread at most)
 #define LB_STREAM_THREADS_2 (32 * (1 + LB_STREAM_GROUPS * LB_STREAM_CONSUMER_WARPS))
+#define LB_STREAM_THREADS_CHUNKED (32 * (1 + LB_STREAM_CONSUMER_WARPS_WIDE))
 #ifndef LB_STREAM_MAX_STAGES
 #define LB_STREAM_MAX_STAGES 8
 #endif
@@ -107,7 +111,8 @@ struct StreamShape {
     int grid;
     int groups;          // consumer groups, each folding its own rows
     int consumer_warps;  // warps per group
-    int vpt;             // vectors per consumer thread (1, 2 or 4)
+    int vpt;             // vectors per consumer thread (1, 2; 4 = chunked rows)
+    int chunks;          // stages per row: 1, or 2..4 column chunks when vpt == 4
     int stages;          // 2..8
     int smem_bytes;      // dynamic shared memory per CTA
     int device;          // launch: the current device (-1 if unknown)

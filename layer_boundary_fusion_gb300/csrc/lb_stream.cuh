@@ -224,18 +224,17 @@ struct StageMeta {
 static_assert(sizeof(StageMeta) == LB_STREAM_META_BYTES, "stage metadata size");
 
 // Threads per CTA the kernel is compiled for: one producer warp plus the consumer
-// groups.  Four-vector threads need more registers and run one group.
+// groups.  kVpt == 4 is the chunked-row variant: one group, one vector per chunk.
 template <int kVpt>
 struct StreamThreads {
-    static constexpr int groups = (kVpt >= 4) ? LB_STREAM_GROUPS_WIDE : LB_STREAM_GROUPS;
-    static constexpr int value = 32 * (1 + groups * LB_STREAM_CONSUMER_WARPS);
+    static constexpr bool chunked = kVpt >= 4;
+    static constexpr int value = chunked ? LB_STREAM_THREADS_CHUNKED : LB_STREAM_THREADS_2;
 };
 // Warps of one consumer group at most (the wide-row shapes use up to 16).
 constexpr int kMaxGroupWarps = LB_STREAM_CONSUMER_WARPS > LB_STREAM_CONSUMER_WARPS_WIDE
                                    ? LB_STREAM_CONSUMER_WARPS
                                    : LB_STREAM_CONSUMER_WARPS_WIDE;
-constexpr int kGroupsMax =
-    LB_STREAM_GROUPS > LB_STREAM_GROUPS_WIDE ? LB_STREAM_GROUPS : LB_STREAM_GROUPS_WIDE;
+constexpr int kGroupsMax = LB_STREAM_GROUPS;
 
 // Group-local barrier that also ORs a predicate over the group (barrier id 1 + g).
 __device__ __forceinline__ bool group_sync_or(bool pred, int id, int nthreads) {
@@ -262,6 +261,10 @@ __device__ __forceinline__ bool group_sync_or(bool pred, int id, int nthreads) {
 // and each stage's uses are waited for in order, which the one-bit phase parity of
 // an mbarrier wait requires (a group that skipped ahead to use k of a stage whose use
 // k-1 had not landed would see phase k-1's parity as complete).
+// Chunked rows (kVpt == 4): a slot holds one column chunk of 32 x 8 x W elements of an
+// input row, row i's chunk c is stage (i x chunks + c) % stages, and the single group
+// folds the chunks in order; thread t keeps vector t of every chunk in registers
+// until the row's reduction, so the thread-to-column map is the whole-row one.
 template <int kMode, bool kFp8, int kVpt>
 __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
     stream_kernel(const __grid_constant__ Params p) {
@@ -277,7 +280,11 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
     const bool has_res = p.residual_in != nullptr;
     const int n_main = (kMode == kFold) ? p.K : p.topk;
     const int n_slots = n_main + (has_res ? 1 : 0);
-    const uint32_t slot_bytes = static_cast<uint32_t>(p.H * 2);
+    constexpr bool kChunked = StreamThreads<kVpt>::chunked;
+    // elements of an input row per stage, and stages per row
+    const int64_t chunk = kChunked ? static_cast<int64_t>(W) * 256 : p.H;
+    const int nch = kChunked ? static_cast<int>((p.H + chunk - 1) / chunk) : 1;
+    const uint32_t slot_bytes = static_cast<uint32_t>(chunk * 2);
     const uint32_t stage_bytes = slot_bytes * n_slots;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + static_cast<size_t>(ns) * stage_bytes);
     const uint32_t full0 = smem_addr(bars);
@@ -285,12 +292,18 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
     const uint32_t stage0 = smem_addr(smem);
     // MoE: per row, its expert indices and routing weights (cp.async by the producer,
     // d <= ns rows ahead) and the mask of valid indices (written before the producer
-    // arms the stage's "full" barrier).  Row i uses block i % (2 ns): the block of row
-    // i + d last served row i + d - 2 ns, whose stage has since been released and
-    // reissued (row i + d - ns < i), so it is free when the fetch is issued.
+    // arms the row's first "full" barrier).  Row i uses block i % (2 ns): the block of
+    // row i + d last served row i + d - 2 ns, whose last stage lies at least ns stage
+    // uses before row i's last one and was released before that one was issued, so
+    // it is free when the fetch is issued (and when row i's mask is written).
     StageMeta *meta = reinterpret_cast<StageMeta *>(bars + 2 * ns);
+    // Chunked rows: the read weight (gamma, or 1 + gamma) after the metadata ring, H
+    // floats; each consumer thread writes and reads back only its own vectors' eight,
+    // which keeps them out of the registers that the four folded vectors need.
+    float4 *wsm = reinterpret_cast<float4 *>(meta + 2 * ns);
 
-    if (G < 1 || ns % G != 0) {                           // launch contract, see above
+    if (G < 1 || ns % G != 0 || nch > (kChunked ? kVpt : 1) ||
+        (kChunked && G != 1)) {                          // launch contract, see above
         if (threadIdx.x == 0)
             atomicOr(&g_device_error, kDeviceErrLaunch);
         return;
@@ -352,57 +365,70 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
         const int ahead_rows = ns < LB_MOE_META_AHEAD ? ns : LB_MOE_META_AHEAD;
         for (int b = 0; b < ahead_rows; ++b)
             fetch_meta(b);
-        int s = 0;                       // stage of the next row to issue
+        int s = 0;                       // stage of the next chunk to issue
         uint32_t k = 0;                  // use of that stage
+        int units = 0;                   // chunks issued (one per row unless chunked)
         for (; row < rows; ++issued) {
-            bool free_ok = true;
-            if (k > 0 && lane == 0)
-                free_ok = mbar_wait_bounded(empty0 + 8 * s, (k - 1) & 1u, &abort_flag);
-            if (!__shfl_sync(0xFFFFFFFFu, free_ok, 0)) {
-                ok = false;
-                break;
-            }
-            const uint32_t full = full0 + 8 * s;
-            const int blk = s + ns * static_cast<int>(k & 1u);
-            // sources of this row: lane j handles slot j (n_slots <= 17 <= 32)
+            const int blk = issued % (2 * ns);          // this row's metadata block
             const void *src = nullptr;
-            if (kMode == kMoe && lane < n_main) {
-                cp_async_wait_pending(ahead_rows - 1);   // this row's group landed
-                const int32_t e = meta[blk].idx[lane];
-                if (e >= 0 && static_cast<int64_t>(e) < n_experts)
-                    src = experts + static_cast<int64_t>(e) * H;
-            } else if (lane_base != nullptr) {
-                src = lane_base + (lane_row0 + row) * H;
-            }
-            const unsigned valid = __ballot_sync(0xFFFFFFFFu, src != nullptr);
-            if (kMode == kMoe) {
-                if (lane == 0) {
-                    const unsigned main_mask = (n_main >= 32) ? 0xFFFFFFFFu : ((1u << n_main) - 1u);
-                    meta[blk].valid = valid & main_mask;
-                    if ((valid & main_mask) != main_mask && p.bad_index != nullptr)
-                        *p.bad_index = 1;
+            unsigned valid = 0;
+            for (int c = 0; c < nch; ++c) {
+                bool free_ok = true;
+                if (k > 0 && lane == 0)
+                    free_ok = mbar_wait_bounded(empty0 + 8 * s, (k - 1) & 1u, &abort_flag);
+                if (!__shfl_sync(0xFFFFFFFFu, free_ok, 0)) {
+                    ok = false;
+                    break;
                 }
-                __syncwarp();
-            }
-            if (lane == 0)
-                mbar_arrive_expect_tx(full, slot_bytes * __popc(valid));
+                if (c == 0) {
+                    // sources of this row: lane j handles slot j (n_slots <= 17 <= 32)
+                    if (kMode == kMoe && lane < n_main) {
+                        cp_async_wait_pending(ahead_rows - 1);   // this row's group landed
+                        const int32_t e = meta[blk].idx[lane];
+                        if (e >= 0 && static_cast<int64_t>(e) < n_experts)
+                            src = experts + static_cast<int64_t>(e) * H;
+                    } else if (lane_base != nullptr) {
+                        src = lane_base + (lane_row0 + row) * H;
+                    }
+                    valid = __ballot_sync(0xFFFFFFFFu, src != nullptr);
+                    if (kMode == kMoe) {
+                        if (lane == 0) {
+                            const unsigned main_mask =
+                                (n_main >= 32) ? 0xFFFFFFFFu : ((1u << n_main) - 1u);
+                            meta[blk].valid = valid & main_mask;
+                            if ((valid & main_mask) != main_mask && p.bad_index != nullptr)
+                                *p.bad_index = 1;
+                        }
+                        __syncwarp();
+                    }
+                }
+                const uint32_t full = full0 + 8 * s;
+                const int64_t c0 = static_cast<int64_t>(c) * chunk;    // first column
+                const uint32_t bytes =
+                    static_cast<uint32_t>((H - c0 < chunk ? H - c0 : chunk) * 2);
+                if (lane == 0)
+                    mbar_arrive_expect_tx(full, bytes * __popc(valid));
 #ifdef LB_TEST_HOOKS
-            if (row == p.test_withhold_row)
-                src = nullptr;                   // the posted bytes never arrive
+                if (row == p.test_withhold_row)
+                    src = nullptr;               // the posted bytes never arrive
 #endif
-            const uint32_t dst = stage0 + static_cast<uint32_t>(s) * stage_bytes;
-            for (int j = 0; j < n_slots; ++j) {
-                const void *sj = reinterpret_cast<const void *>(
-                    __shfl_sync(0xFFFFFFFFu, reinterpret_cast<unsigned long long>(src), j));
-                if (lane == 0 && sj != nullptr)
-                    bulk_g2s(dst + j * slot_bytes, sj, slot_bytes, full);
+                const uint32_t dst = stage0 + static_cast<uint32_t>(s) * stage_bytes;
+                for (int j = 0; j < n_slots; ++j) {
+                    const uint16_t *sj = reinterpret_cast<const uint16_t *>(__shfl_sync(
+                        0xFFFFFFFFu, reinterpret_cast<unsigned long long>(src), j));
+                    if (lane == 0 && sj != nullptr)
+                        bulk_g2s(dst + j * slot_bytes, sj + c0, bytes, full);
+                }
+                ++units;
+                if (++s == ns) {
+                    s = 0;
+                    ++k;
+                }
             }
+            if (!ok)
+                break;
             row = next_row(p, row + gridDim.x);
             fetch_meta((issued + ahead_rows) % (2 * ns));   // block of row i + ahead_rows
-            if (++s == ns) {
-                s = 0;
-                ++k;
-            }
         }
         if (kMode == kMoe)
             cp_async_wait_pending(0);    // no metadata copy outlives the CTA
@@ -412,9 +438,9 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
         }
         // Drain: the copies of the last stages issued must land before the CTA ends.
         if (lane == 0) {
-            const int first = issued > ns ? issued - ns : 0;
-            for (int i = first; i < issued; ++i)
-                if (!mbar_wait_bounded(full0 + 8 * (i % ns), (i / ns) & 1u, nullptr))
+            const int first = units > ns ? units - ns : 0;
+            for (int u = first; u < units; ++u)
+                if (!mbar_wait_bounded(full0 + 8 * (u % ns), (u / ns) & 1u, nullptr))
                     atomicOr(&g_device_error, kDeviceErrTimeout);
         }
         return;
@@ -437,50 +463,54 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
         const int64_t v = ct + static_cast<int64_t>(i) * gthreads;
         act[i] = v < nvec;
         col[i] = v * 8;
-        soff[i] = static_cast<uint32_t>(v * 16);
+        // chunked rows: vector i is vector ct of chunk i
+        soff[i] = static_cast<uint32_t>((kChunked ? ct : v) * 16);
     }
     pdl_wait();
 #pragma unroll
     for (int i = 0; i < kVpt; ++i) {
         if (act[i] && need_read) {
-            const float4 a = __ldg(reinterpret_cast<const float4 *>(p.gamma + col[i]));
-            const float4 b = __ldg(reinterpret_cast<const float4 *>(p.gamma + col[i]) + 1);
-            gm[i][0] = make_float2(a.x, a.y);
-            gm[i][1] = make_float2(a.z, a.w);
-            gm[i][2] = make_float2(b.x, b.y);
-            gm[i][3] = make_float2(b.z, b.w);
+            float4 a = __ldg(reinterpret_cast<const float4 *>(p.gamma + col[i]));
+            float4 b = __ldg(reinterpret_cast<const float4 *>(p.gamma + col[i]) + 1);
             if (p.gemma) {                         // GemmaRMSNorm: weight = 1 + gamma
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    gm[i][e] = __fadd2_rn(make_float2(1.0f, 1.0f), gm[i][e]);
+                a = make_float4(1.0f + a.x, 1.0f + a.y, 1.0f + a.z, 1.0f + a.w);
+                b = make_float4(1.0f + b.x, 1.0f + b.y, 1.0f + b.z, 1.0f + b.w);
             }
-        } else {
+            if (kChunked) {
+                wsm[col[i] >> 2] = a;
+                wsm[(col[i] >> 2) + 1] = b;
+            } else {
+                gm[i][0] = make_float2(a.x, a.y);
+                gm[i][1] = make_float2(a.z, a.w);
+                gm[i][2] = make_float2(b.x, b.y);
+                gm[i][3] = make_float2(b.z, b.w);
+            }
+        } else if (!kChunked) {
 #pragma unroll
             for (int e = 0; e < 4; ++e)
                 gm[i][e] = make_float2(0.0f, 0.0f);
         }
     }
+    // the weight of vector v's elements 2e, 2e + 1
+    auto weight = [&](int v, int e) -> float2 {
+        if (!kChunked)
+            return gm[v][e];
+        const float4 t = wsm[(col[v] >> 2) + (e >> 1)];
+        return (e & 1) ? make_float2(t.z, t.w) : make_float2(t.x, t.y);
+    };
 
     // This group's rows are the CTA's valid rows g, g + G, g + 2G, ...; with the
-    // stage count a multiple of G, the group's stage advances by G per row and the
-    // phase parity flips each time it wraps.
+    // stage count a multiple of G, the group's stage advances by G per stage use (one
+    // use per row, or per chunk of a chunked row with G = 1) and the phase parity
+    // flips each time it wraps.
     int s = g;
     uint32_t phase = 0;
     int par = 0;
+    int blk = g;                                         // this row's metadata block
     int64_t row = next_row(p, blockIdx.x);
     for (int t = 0; t < g && row < p.rows; ++t)
         row = next_row(p, row + gridDim.x);
-    for (; row < p.rows; s += G) {
-        if (s >= ns) {
-            s -= ns;
-            phase ^= 1u;
-        }
-        const uint32_t k = phase;
-        const int blk = s + ns * static_cast<int>(phase);   // this row's metadata block
-
-        // A thread whose wait fails reads nothing from the stage and writes nothing;
-        // the group learns of it at its row barrier and leaves together.
-        const bool ok = mbar_wait_bounded(full0 + 8 * s, k & 1u, &abort_flag);
+    for (; row < p.rows; blk = (blk + G < 2 * ns) ? blk + G : blk + G - 2 * ns) {
         // o in binary32 pairs: acc[v][i] holds elements 2i, 2i+1 of vector v.  Mixed
         // add.rn.f32.bf16 adds, scalar mul.rn products and packed f32x2 adds all round
         // like the scalar binary32 ops, so the order of the definition -- and residual'
@@ -491,55 +521,70 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
 #pragma unroll
             for (int e = 0; e < 4; ++e)
                 acc[v][e] = make_float2(0.0f, 0.0f);
-        if (ok) {
-            const uint32_t stage = stage0 + static_cast<uint32_t>(s) * stage_bytes;
-            const uint32_t valid = (kMode == kMoe) ? meta[blk].valid : 0u;
+        // A thread whose wait fails reads nothing from the stage and writes nothing;
+        // the group learns of it at its row barrier and leaves together.
+        bool ok = true;
 #pragma unroll
-            for (int j = 0; j < LB_MAX_K; ++j) {
-                if (j >= n_main)
-                    break;
-                if (kMode == kMoe && !((valid >> j) & 1u))
-                    continue;
-                const float wj = (kMode == kMoe) ? meta[blk].w[j] : 1.0f;
-                const uint32_t slot = stage + static_cast<uint32_t>(j) * slot_bytes;
+        for (int c = 0; c < (kChunked ? kVpt : 1); ++c) {
+            if (c >= nch)
+                break;
+            if (s >= ns) {
+                s -= ns;
+                phase ^= 1u;
+            }
+            if (ok)
+                ok = mbar_wait_bounded(full0 + 8 * s, phase, &abort_flag);
+            if (ok) {
+                const uint32_t stage = stage0 + static_cast<uint32_t>(s) * stage_bytes;
+                const uint32_t valid = (kMode == kMoe) ? meta[blk].valid : 0u;
+#pragma unroll
+                for (int j = 0; j < LB_MAX_K; ++j) {
+                    if (j >= n_main)
+                        break;
+                    if (kMode == kMoe && !((valid >> j) & 1u))
+                        continue;
+                    const float wj = (kMode == kMoe) ? meta[blk].w[j] : 1.0f;
+                    const uint32_t slot = stage + static_cast<uint32_t>(j) * slot_bytes;
+#pragma unroll
+                    for (int v = 0; v < kVpt; ++v)
+                        if ((!kChunked || v == c) && act[v]) {
+                            const uint4 x = lds128(slot + soff[v]);
+                            if (kMode == kMoe) {
+                                float2 f[4];
+                                unpack8x2(x, f);
+#pragma unroll
+                                for (int e = 0; e < 4; ++e)
+                                    acc[v][e] = add_mul2_rn(acc[v][e], wj, f[e]);
+                            } else {
+                                add_bf16x8(acc[v], x);
+                            }
+                        }
+                }
+                if (has_res) {
+                    const uint32_t slot = stage + static_cast<uint32_t>(n_main) * slot_bytes;
+#pragma unroll
+                    for (int v = 0; v < kVpt; ++v)
+                        if ((!kChunked || v == c) && act[v])
+                            add_bf16x8(acc[v], lds128(slot + soff[v]));
+                }
+            }
+            // the stage's data is in registers: hand it back to the producer
+            __syncwarp();
+            if (ok && lane == 0)
+                mbar_arrive(empty0 + 8 * s);
+            s += G;
+            if (ok && (p.residual_out != nullptr || p.snapshot != nullptr)) {
+                const int64_t roff = row * p.H;
 #pragma unroll
                 for (int v = 0; v < kVpt; ++v)
-                    if (act[v]) {
-                        const uint4 x = lds128(slot + soff[v]);
-                        if (kMode == kMoe) {
-                            float2 f[4];
-                            unpack8x2(x, f);
-#pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                acc[v][e] = add_mul2_rn(acc[v][e], wj, f[e]);
-                        } else {
-                            add_bf16x8(acc[v], x);
-                        }
+                    if ((!kChunked || v == c) && act[v]) {
+                        const uint4 packed = pack8x2(acc[v]);
+                        if (p.residual_out != nullptr)
+                            st_stream16(p.residual_out + roff + col[v], packed);
+                        if (p.snapshot != nullptr)
+                            *reinterpret_cast<uint4 *>(p.snapshot + roff + col[v]) = packed;
                     }
             }
-            if (has_res) {
-                const uint32_t slot = stage + static_cast<uint32_t>(n_main) * slot_bytes;
-#pragma unroll
-                for (int v = 0; v < kVpt; ++v)
-                    if (act[v])
-                        add_bf16x8(acc[v], lds128(slot + soff[v]));
-            }
-        }
-        // the stage's data is in registers: hand it back to the producer
-        __syncwarp();
-        if (ok && lane == 0)
-            mbar_arrive(empty0 + 8 * s);
-        const int64_t roff = row * p.H;
-        if (ok && (p.residual_out != nullptr || p.snapshot != nullptr)) {
-#pragma unroll
-            for (int v = 0; v < kVpt; ++v)
-                if (act[v]) {
-                    const uint4 packed = pack8x2(acc[v]);
-                    if (p.residual_out != nullptr)
-                        st_stream16(p.residual_out + roff + col[v], packed);
-                    if (p.snapshot != nullptr)
-                        *reinterpret_cast<uint4 *>(p.snapshot + roff + col[v]) = packed;
-                }
         }
         if (!need_read) {
             if (!ok) {
@@ -551,6 +596,7 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
             continue;
         }
 
+        const int64_t roff = row * p.H;
         // One barrier per row: sum(o^2) and, for FP8, max|o * gamma| (amax of the read
         // is r * max|o * gamma| since r > 0), plus the group's verdict on the waits.
         float2 ss2 = make_float2(0.0f, 0.0f);
@@ -562,7 +608,7 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
                 for (int e = 0; e < 4; ++e) {
                     ss2 = __ffma2_rn(acc[v][e], acc[v][e], ss2);
                     if (kFp8) {
-                        const float2 t = __fmul2_rn(acc[v][e], gm[v][e]);
+                        const float2 t = __fmul2_rn(acc[v][e], weight(v, e));
                         mg = fmaxf(mg, fmaxf(fabsf(t.x), fabsf(t.y)));
                     }
                 }
@@ -595,12 +641,14 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
         const float r = rsqrtf(__fmaf_rn(ss, p.inv_H, p.eps));
         const float2 r2 = make_float2(r, r);
 
-        // yf = (o * r) * gamma
+        // yf = (o * r) * gamma, for this thread's vectors of the row only (a chunked
+        // row keeps no weight for the others)
 #pragma unroll
         for (int v = 0; v < kVpt; ++v)
+            if (act[v])
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                acc[v][e] = __fmul2_rn(__fmul2_rn(acc[v][e], r2), gm[v][e]);
+                for (int e = 0; e < 4; ++e)
+                    acc[v][e] = __fmul2_rn(__fmul2_rn(acc[v][e], r2), weight(v, e));
 
         if (p.y_out != nullptr) {
 #pragma unroll

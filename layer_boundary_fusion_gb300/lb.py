@@ -55,7 +55,7 @@ class Plan(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int), ("grid", ctypes.c_int), ("threads", ctypes.c_int),
                 ("vectors_per_thread", ctypes.c_int), ("ctas_per_row", ctypes.c_int),
                 ("stages", ctypes.c_int), ("smem_bytes", ctypes.c_int),
-                ("groups", ctypes.c_int)]
+                ("groups", ctypes.c_int), ("chunks", ctypes.c_int)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}

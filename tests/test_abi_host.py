@@ -82,7 +82,11 @@ SMEM = 232448          # opt-in shared memory per CTA on GB300
     (4096, 8192, 5, (1, 152, 544, 2, 1, 2, 164448)),    # one group of 16 warps
     (4096, 6144, 2, (1, 152, 800, 2, 1, 8, 199040)),    # two groups of 12 warps
     (4096, 8192, 9, (0, 4096, 512, 2, 1, 0, 0)),        # no double-buffered stage fits
-    (4096, 16384, 3, (0, 4096, 512, 4, 1, 0, 0)),
+    (4096, 4096, 17, (0, 4096, 512, 1, 1, 0, 0)),
+    (4096, 8200, 17, (1, 152, 352, 4, 1, 2, 207488)),   # 4 chunks of 10 warps
+    (4096, 12288, 5, (1, 152, 544, 4, 1, 4, 214208)),   # 3 chunks of 16 warps
+    (4096, 16384, 3, (1, 152, 544, 4, 1, 6, 214816)),   # 4 chunks
+    (4096, 16384, 17, (0, 4096, 512, 4, 1, 0, 0)),      # no chunked stage fits twice
     (4096, 32768, 2, (0, 8192, 512, 4, 2, 0, 0)),
     (4096, 520, 2, (1, 152, 416, 1, 1, 6, 14304)),      # 65 vectors: partly active warp
     (4096, 8, 2, (1, 152, 224, 1, 1, 6, 2016)),
@@ -112,13 +116,20 @@ def test_launch_plan_covers_every_row_vector(lib):
                     consumers = (p.threads - 32) // groups
                     assert consumers * groups + 32 == p.threads
                     assert consumers % 64 == 0 and 64 <= consumers <= 512
-                    assert consumers * p.vectors_per_thread >= nvec
-                    if consumers > 256:          # wide groups keep two vectors a thread
-                        assert p.vectors_per_thread == 2
                     assert 2 <= p.stages <= 8 and p.grid == min(rows, 152)
                     # every stage belongs to one consumer group
                     assert p.stages % groups == 0
-                    assert p.smem_bytes == p.stages * (n_in * H * 2 + 16 + 2 * 144)
+                    if p.chunks == 1:            # whole rows: 1 or 2 vectors a thread
+                        assert p.vectors_per_thread in (1, 2)
+                        assert consumers * p.vectors_per_thread >= nvec
+                        width, weight = H, 0
+                    else:                        # chunks of one vector per thread
+                        assert p.vectors_per_thread == 4 and groups == 1
+                        assert 2 <= p.chunks <= 4
+                        assert (p.chunks - 1) * consumers < nvec <= p.chunks * consumers
+                        width, weight = consumers * 8, H * 4
+                    assert p.smem_bytes == (p.stages * (n_in * width * 2 + 16 + 2 * 144)
+                                            + weight)
                     assert p.smem_bytes + 1024 <= SMEM
                 assert p.vectors_per_thread in (1, 2, 4)
 

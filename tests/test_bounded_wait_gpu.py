@@ -31,7 +31,7 @@ from parity_util import Guarded, dev_bits, f32
 L = lb.load(build.build(test_hooks=True))
 L.lb_test_withhold_row.argtypes = [ctypes.c_int64]
 L.lb_test_withhold_row.restype = None
-K, T, H, eps, ROW = 2, 300, 1024, 1e-6, 5
+K, T, H, eps, ROW = 2, 300, int(sys.argv[2]), 1e-6, 5
 w = wl.fold_workload("timeout", K, T, H, seed=77)
 want = oracle.fold_norm(w.partials, w.residual, w.gamma, eps)
 P = [dev_bits(p) for p in w.partials]
@@ -73,20 +73,21 @@ own = [t for t in range(T) if t % plan.grid == cta]
 ro2, yo2 = call()
 err2 = lb.lb_device_error(clear=True)
 state2 = rows_state(ro2, yo2)
-print(json.dumps({"kernel": plan.kernel, "err": err, "elapsed": elapsed,
+print(json.dumps({"kernel": plan.kernel, "chunks": plan.chunks, "err": err, "elapsed": elapsed,
                   "row": state[ROW], "others_ok": all(state[t] == "ok" for t in range(T) if t not in own),
                   "own": [state[t] for t in own], "err2": err2,
                   "after_ok": all(s == "ok" for s in state2)}))
 """
 
 
-def test_a_withheld_row_times_out_and_the_context_survives():
-    r = subprocess.run([sys.executable, "-c", _SCRIPT, ROOT], capture_output=True, text=True,
-                       timeout=600)
+@pytest.mark.parametrize("H,chunks", [(1024, 1), (12288, 3)])   # whole rows, chunked rows
+def test_a_withheld_row_times_out_and_the_context_survives(H, chunks):
+    r = subprocess.run([sys.executable, "-c", _SCRIPT, ROOT, str(H)], capture_output=True,
+                       text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-4000:]
     got = json.loads(r.stdout.strip().splitlines()[-1])
     from layer_boundary_fusion_gb300 import lb
-    assert got["kernel"] == lb.LB_KERNEL_STREAM
+    assert got["kernel"] == lb.LB_KERNEL_STREAM and got["chunks"] == chunks
     assert got["err"] & lb.LB_DEVICE_ERR_TIMEOUT
     assert 0.5 < got["elapsed"] < 60.0               # the wait ran out after about a second
     assert got["row"] == "untouched"                 # the withheld row was never written

@@ -223,7 +223,10 @@ def test_moe_finalize_fp8_and_initial(lb):
 
 @pytest.mark.parametrize("T,H,E,topk", [(1, 4096, 16, 16), (37, 520, 8, 3), (64, 8192, 64, 8),
                                         (5, 16384, 8, 1), (200, 1024, 16, 16),
-                                        (1, 2048, 128, 8)])
+                                        (1, 2048, 128, 8),
+                                        (300, 8192, 64, 8),     # row kernel past the SMs
+                                        (200, 12288, 16, 4),    # stream kernel, 3 chunks
+                                        (160, 10240, 32, 8)])   # 3 chunks, the last short
 def test_moe_shapes(lb, T, H, E, topk):
     w = wl.moe_workload("m", T, H, E, topk, seed=T + H)
     want = oracle.moe_finalize_fold_norm(w.expert_out, w.idx, w.w, w.residual, w.gamma, w.eps)
@@ -271,14 +274,14 @@ def test_stream_modes(lb):
     check_fold(got, full, "in place")
 
 
-@pytest.mark.parametrize("T", [50, 700])
-def test_stream_modes_on_both_kernels(lb, T):
-    """The same stream modes with enough rows for the persistent TMA kernel (T=700)
-    and few enough for the row kernel (T=50)."""
-    w = wl.fold_workload("modes2", 3, T, 2048, seed=52 + T)
+@pytest.mark.parametrize("T,H", [(50, 2048), (700, 2048), (300, 12288)])
+def test_stream_modes_on_both_kernels(lb, T, H):
+    """The same stream modes with enough rows for the persistent TMA kernel (T=700;
+    T=300 with rows in column chunks) and few enough for the row kernel (T=50)."""
+    w = wl.fold_workload("modes2", 3, T, H, seed=52 + T)
     kernel = lb.LB_KERNEL_STREAM if T >= torch.cuda.get_device_properties(0) \
         .multi_processor_count else lb.LB_KERNEL_ROW
-    assert plan(lb, T, 2048, 4).kernel == kernel
+    assert plan(lb, T, H, 4).kernel == kernel
     full = oracle.fold_norm(w.partials, w.residual, w.gamma, w.eps, want_fp8=True)
     init = oracle.fold_norm(w.partials, None, w.gamma, w.eps, want_fp8=True)
     check_fold(gpu_fold(lb, w.partials, None, w.gamma, w.eps), init, "enter")
@@ -365,6 +368,8 @@ def test_specified_workloads_take_the_intended_kernels(lb):
     p = plan(lb, 64, 4096, 9)                                        # decode
     assert p.kernel == lb.LB_KERNEL_ROW and p.grid == 64
     assert plan(lb, 4, 32768, 2).ctas_per_row == 2                   # long rows: cluster
+    p = plan(lb, 2048, 12288, 5)                                     # wide prefill
+    assert p.kernel == lb.LB_KERNEL_STREAM and p.chunks == 3
 
 
 # --------------------------------------------------------------------------------------
@@ -389,11 +394,17 @@ def test_specified_workloads_take_the_intended_kernels(lb):
     (3, 151, 4096),     # one row short of the SM count: row kernel
     (3, 153, 8),        # stream kernel, one vector per row, a ragged wave
     (16, 160, 24),      # stream kernel, maximum K, three vectors per row
-    (2, 200, 12288),    # row kernel beyond the SM count (rows too long to stage)
+    (2, 200, 12288),    # stream kernel, rows in 3 column chunks
     (2, 30000, 256),    # stream kernel, ~200 rows per CTA: every stage wraps many times
     (4, 300, 5120),     # stream kernel, two groups of 10 warps
     (4, 300, 6144),     # stream kernel, two groups of 12 warps
     (3, 200, 7168),     # stream kernel, one group of 14 warps
+    (4, 300, 12288),    # stream kernel, 3 chunks of 16 warps
+    (2, 160, 16384),    # stream kernel, 4 chunks of 16 warps
+    (3, 160, 10240),    # stream kernel, 3 chunks of 14 warps, the last one short
+    (8, 200, 8192),     # row kernel: whole rows of 9 inputs do not double-buffer
+    (16, 153, 8200),    # stream kernel, maximum K, 4 chunks of 10 warps, 65 vectors in the last
+    (8, 160, 12288),    # stream kernel, 3 chunks of 16 warps, 2 stages
 ])
 def test_shapes(lb, K, T, H):
     w = wl.fold_workload("shape", K, T, H, seed=K * 1000 + T + H)
@@ -478,10 +489,10 @@ def _options_fold(lb, w, *, fp8, gemma, snapshot):
     return {k: g.host() for k, g in out.items()}
 
 
-@pytest.mark.parametrize("T", [50, 700])
+@pytest.mark.parametrize("T,H", [(50, 2048), (700, 2048), (200, 12288)])   # chunked rows last
 @pytest.mark.parametrize("fp8", [False, True])
-def test_gemma_weight_and_snapshot(lb, T, fp8):
-    w = wl.fold_workload("gem", 3, T, 2048, seed=93 + T)
+def test_gemma_weight_and_snapshot(lb, T, H, fp8):
+    w = wl.fold_workload("gem", 3, T, H, seed=93 + T)
     w.gamma = (0.05 * np.random.default_rng(T).standard_normal(w.H)).astype(np.float32)
     want = oracle.fold_norm(w.partials, w.residual, w.gamma, w.eps, want_fp8=True, gemma=True)
     got = _options_fold(lb, w, fp8=fp8, gemma=True, snapshot=True)

@@ -35,7 +35,8 @@ def lb():
 
 
 def _draw_shape(rng):
-    H = int(rng.choice([8, 24, 64, 520, 1024, 2048, 2056, 4096, 6144, 8192, 12288, 16384]))
+    H = int(rng.choice([8, 24, 64, 520, 1024, 2048, 2056, 4096, 6144, 8192, 10240, 12288,
+                          16384]))
     T = int(rng.choice([1, 3, 17, 64, 151, 152, 153, 300, 777, 1500]))
     while T * H > MAX_ELEMS and T > 1:
         T //= 2
