@@ -1,10 +1,11 @@
 """Run one boundary workload a few times, for profilers (ncu) and quick timing.
 
     python -m layer_boundary_fusion_gb300.profile_case prefill_fold_norm_fp8 \
-        --launches 4 [--row-scale 3] [--sets 2]
+        --launches 4 [--row-scale 3] [--sets 2] [--hidden 12288]
 
-Builds the seeded workload, optionally repeats its rows `--row-scale` times (so that a
-capture's working set exceeds the L2 cache), and launches the boundary call
+Builds the seeded workload (the prefill one optionally at another hidden size),
+optionally repeats its rows `--row-scale` times (so that a capture's working set
+exceeds the L2 cache), and launches the boundary call
 `--launches` times, rotating over `--sets` independent buffer sets.  Prints the mean
 time per launch measured with CUDA events (not meaningful under a profiler).
 """
@@ -25,8 +26,8 @@ def _bits(a, dev):
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
 
 
-def make_launcher(name, row_scale, dev, stream):
-    w = wl.WORKLOADS[name]()
+def make_launcher(name, row_scale, dev, stream, hidden=None):
+    w = wl.prefill_fold_norm_fp8(H=hidden) if hidden else wl.WORKLOADS[name]()
     sp = stream.cuda_stream
     G = torch.from_numpy(w.gamma).to(dev)
     if name == "moe_finalize":
@@ -67,11 +68,16 @@ def main(argv=None):
     ap.add_argument("--launches", type=int, default=4)
     ap.add_argument("--row-scale", type=int, default=1)
     ap.add_argument("--sets", type=int, default=2)
+    ap.add_argument("--hidden", type=int, default=None,
+                    help="prefill_fold_norm_fp8 only: hidden size (default 4096)")
     a = ap.parse_args(argv)
+    if a.hidden is not None and a.workload != "prefill_fold_norm_fp8":
+        ap.error("--hidden applies to prefill_fold_norm_fp8 only")
     dev = torch.device("cuda", 0)
     lb.load()
     stream = torch.cuda.Stream(dev)
-    runs = [make_launcher(a.workload, a.row_scale, dev, stream) for _ in range(a.sets)]
+    runs = [make_launcher(a.workload, a.row_scale, dev, stream, a.hidden)
+            for _ in range(a.sets)]
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)

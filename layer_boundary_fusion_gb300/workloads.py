@@ -175,10 +175,11 @@ def decode_fold_norm(seed=1, initial=False):
                          4096, seed, partial_std=0.5, residual=not initial)
 
 
-def prefill_fold_norm_fp8(seed=2):
+def prefill_fold_norm_fp8(seed=2, H=4096):
     """K=4 partials [2048,4096] ~N(0,1) with 1% of rows x50, residual ~N(0,1),
-    RMSNorm then per-token dynamic FP8 E4M3."""
-    return fold_workload("prefill_fold_norm_fp8", 4, 2048, 4096, seed,
+    RMSNorm then per-token dynamic FP8 E4M3.  (Another H gives the same recipe at that
+    hidden size, for sweeps and profiles of other widths.)"""
+    return fold_workload("prefill_fold_norm_fp8", 4, 2048, H, seed,
                          outlier_frac=0.01, fp8=True)
 
 
