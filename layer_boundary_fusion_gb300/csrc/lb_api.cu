@@ -303,6 +303,8 @@ bool choose_stream_shape(int64_t rows, int64_t H, int n_inputs, int num_sms,
         num_sms <= 0)
         return false;
     const int64_t nvec = H / 8;
+    if (nvec <= LB_STREAM_MIN_ROW_VECS)
+        return false;                          // short rows: the row kernel measured faster
     const int64_t wide = LB_STREAM_CONSUMER_WARPS_WIDE;
     int64_t per_cta = LB_SMEM_PER_SM / LB_STREAM_CTAS_PER_SM - 1024;
     if (per_cta > smem_per_block)

@@ -35,6 +35,16 @@
 // (1 or 2 vectors per thread) and chunked rows (4 chunks per thread at most)
 #define LB_STREAM_THREADS_2 (32 * (1 + LB_STREAM_GROUPS * LB_STREAM_CONSUMER_WARPS))
 #define LB_STREAM_THREADS_CHUNKED (32 * (1 + LB_STREAM_CONSUMER_WARPS_WIDE))
+// Stream-kernel slots of at most this many bytes (one input row, or chunk, per slot)
+// are copied by one producer lane each, larger ones by lane 0 in turn.
+#ifndef LB_STREAM_LANE_ISSUE_BYTES
+#define LB_STREAM_LANE_ISSUE_BYTES 4096
+#endif
+// Rows of at most this many 16-byte vectors take the row kernel at any row count: the
+// stream kernel's per-row copies cost more than such rows carry.
+#ifndef LB_STREAM_MIN_ROW_VECS
+#define LB_STREAM_MIN_ROW_VECS 128
+#endif
 #ifndef LB_STREAM_MAX_STAGES
 #define LB_STREAM_MAX_STAGES 8
 #endif

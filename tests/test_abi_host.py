@@ -88,8 +88,9 @@ SMEM = 232448          # opt-in shared memory per CTA on GB300
     (4096, 16384, 3, (1, 152, 544, 4, 1, 6, 214816)),   # 4 chunks
     (4096, 16384, 17, (0, 4096, 512, 4, 1, 0, 0)),      # no chunked stage fits twice
     (4096, 32768, 2, (0, 8192, 512, 4, 2, 0, 0)),
-    (4096, 520, 2, (1, 152, 416, 1, 1, 6, 14304)),      # 65 vectors: partly active warp
-    (4096, 8, 2, (1, 152, 224, 1, 1, 6, 2016)),
+    (4096, 520, 2, (0, 4096, 96, 1, 1, 0, 0)),          # short rows: row kernel at any T
+    (4096, 8, 2, (0, 4096, 32, 1, 1, 0, 0)),
+    (4096, 1032, 2, (1, 152, 608, 1, 1, 6, 26592)),     # 129 vectors: partly active warp
 ])
 def test_launch_plan(lib, rows, H, n_in, plan):
     p = lib.lb_launch_plan(rows, H, n_in, 152, SMEM)
@@ -111,6 +112,7 @@ def test_launch_plan_covers_every_row_vector(lib):
                     assert p.ctas_per_row * per_cta >= nvec and 1 <= p.ctas_per_row <= 8
                     assert p.grid == rows * p.ctas_per_row
                 else:
+                    assert nvec > 128              # short rows never stream
                     groups = p.groups
                     assert 1 <= groups <= min(3, p.stages) and p.threads <= 800
                     consumers = (p.threads - 32) // groups

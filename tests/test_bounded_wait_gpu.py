@@ -80,7 +80,8 @@ print(json.dumps({"kernel": plan.kernel, "chunks": plan.chunks, "err": err, "ela
 """
 
 
-@pytest.mark.parametrize("H,chunks", [(1024, 1), (12288, 3)])   # whole rows, chunked rows
+@pytest.mark.parametrize("H,chunks", [(2048, 1), (4096, 1), (12288, 3)])
+# whole rows with a copy per producer lane, whole rows with lane 0 issuing, chunked rows
 def test_a_withheld_row_times_out_and_the_context_survives(H, chunks):
     r = subprocess.run([sys.executable, "-c", _SCRIPT, ROOT, str(H)], capture_output=True,
                        text=True, timeout=600)

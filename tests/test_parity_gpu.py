@@ -303,8 +303,8 @@ def test_stream_modes_on_both_kernels(lb, T, H):
 
 
 def test_moe_bad_index_on_the_stream_kernel(lb):
-    w = wl.moe_workload("bad2", 400, 1024, 16, 4, seed=43)
-    assert plan(lb, 400, 1024, 5).kernel == lb.LB_KERNEL_STREAM
+    w = wl.moe_workload("bad2", 400, 2048, 16, 4, seed=43)
+    assert plan(lb, 400, 2048, 5).kernel == lb.LB_KERNEL_STREAM
     idx = w.idx.copy()
     idx[7, 1] = 1 << 30
     idx[300, 3] = -1
@@ -321,7 +321,7 @@ def test_dependent_chain_of_boundaries(lb):
     partials just before each call (the kernels are programmatic dependents of the
     previous launch, so this checks that every read waits for its producer)."""
     rows = (2048, 64, 700, 1024, 2048)           # stream, row, stream, MoE, stream kernels
-    H = 1024
+    H = 2048
     rng = np.random.default_rng(81)
     gamma = (1 + 0.1 * rng.standard_normal(H)).astype(np.float32)
     res_host = wl.to_bf16_bits(rng.standard_normal((max(rows), H)).astype(np.float32))
@@ -385,17 +385,20 @@ def test_specified_workloads_take_the_intended_kernels(lb):
     (2, 9, 16384),      # four vectors per thread
     (1, 4, 32768),      # four vectors per thread, a row split over a 2-CTA cluster
     (5, 301, 4096),     # K above one load chunk, ragged last wave
-    (4, 2048, 1024),
-    (8, 152, 2048),
+    (4, 2048, 1024),    # row kernel past the SM count (rows of <= 1024 elements)
+    (8, 152, 2048),     # stream kernel, one vector per thread, a copy per producer lane
     (2, 160, 4096),     # stream kernel, one or two rows per CTA
     (4, 1000, 4096),    # stream kernel
-    (16, 300, 1024),    # stream kernel at the maximum K (17 staged rows per stage)
+    (16, 300, 1024),    # row kernel at the maximum K, past the SM count
+    (16, 300, 2048),    # stream kernel at the maximum K (17 staged rows per stage)
     (1, 2, 131072),     # the largest hidden size: a row split over an 8-CTA cluster
     (3, 151, 4096),     # one row short of the SM count: row kernel
-    (3, 153, 8),        # stream kernel, one vector per row, a ragged wave
-    (16, 160, 24),      # stream kernel, maximum K, three vectors per row
+    (3, 153, 8),        # row kernel, one vector per row
+    (16, 160, 24),      # row kernel, maximum K, three vectors per row
+    (3, 153, 1032),     # stream kernel, 129 vectors: a partly active warp, a ragged wave
     (2, 200, 12288),    # stream kernel, rows in 3 column chunks
-    (2, 30000, 256),    # stream kernel, ~200 rows per CTA: every stage wraps many times
+    (2, 30000, 256),    # row kernel, 30000 one-warp CTAs
+    (2, 30000, 1032),   # stream kernel, ~200 rows per CTA: every stage wraps many times
     (4, 300, 5120),     # stream kernel, two groups of 10 warps
     (4, 300, 6144),     # stream kernel, two groups of 12 warps
     (3, 200, 7168),     # stream kernel, one group of 14 warps
@@ -629,7 +632,7 @@ def test_non_finite_inputs_propagate_like_the_oracle(lb):
     """A NaN or an infinity in a partial makes its row's outputs non-finite where the
     definition says so; other rows are unaffected.  Compared as float values
     (NaN == NaN), since NaN payloads need not match."""
-    w = wl.fold_workload("nan", 2, 200, 1024, seed=96)
+    w = wl.fold_workload("nan", 2, 200, 2048, seed=96)
     P = [p.copy() for p in w.partials]
     P[0][3, 10] = 0x7FC0                      # NaN
     P[1][7, 20] = 0x7F80                      # +inf
@@ -666,7 +669,7 @@ def test_residual_stream_through_a_layer_stack(lb, T):
     completed and extended contribution with an FP8 read, fold then a plain read, and a
     MoE handoff consumed by a Gemma final norm.  Each read and the residual after each
     step match the oracle evaluating the same sequence of boundary operations."""
-    H, eps = 1024, 1e-6
+    H, eps = 2048, 1e-6
     fw = wl.fold_workload("stack", 4, T, H, seed=98)
     mw = wl.moe_workload("stack_moe", T, H, 16, 4, seed=99)
     E0, P0, P1, X = fw.partials
@@ -770,7 +773,7 @@ def test_fp8_read_of_near_zero_rows(lb):
     subnormal, its reciprocal overflows) and rows of ordinary size side by side, on both
     kernels: codes and scales match the oracle, which divides by the scale."""
     for T in (100, 300):                       # row kernel, stream kernel
-        w = wl.fold_workload("tiny_rows", 2, T, 1024, seed=97)
+        w = wl.fold_workload("tiny_rows", 2, T, 2048, seed=97)
         P = [p.copy() for p in w.partials]
         R = w.residual.copy()
         rng = np.random.default_rng(5)
