@@ -417,7 +417,36 @@ def measure_variants(lb, dev, stream, dist, steps):
     el, _ = time_graph(ls, steps, 20, stream, dist)
     record("moe_finalize_fp8", w.T, nb8, el, steps, plan_of(lb, w.T, w.H, w.topk + 1, props),
            f"rotated {ns} sets")
+    # with the routing promise (LB_OPT_ROUTING_READY: idx and w are never written by the
+    # kernel before a call, here the previous finalize): the first tokens' routing is
+    # read before the previous launch finishes
+    ls = [(lambda s=s: lb.lb_moe_finalize_fold_norm(s[0], w.expert_out.shape[0], I, Wt, w.topk,
+                                                   s[1], s[2], G, s[3], None, None, w.T, w.H,
+                                                   w.eps, None, stream=sp, routing_ready=True))
+          for s in sets]
+    el, _ = time_graph(ls, steps, 20, stream, dist)
+    record("moe_finalize_routing_ready", w.T, nb, el, steps,
+           plan_of(lb, w.T, w.H, w.topk + 1, props), f"rotated {ns} sets")
     del sets, ls, Q
+    # a decode-size finalize (T=64 tokens of the same routing recipe) on the row kernel,
+    # without and with the routing promise
+    # (each set holds only the 512 expert rows those tokens gather, renumbered)
+    T64 = 64
+    E64 = E0[I[:T64].reshape(-1).long()]
+    I64 = torch.arange(T64 * w.topk, dtype=torch.int32, device=dev).view(T64, w.topk)
+    W64 = Wt[:T64].contiguous()
+    nb64 = bytes_moe(T64, w.H, w.topk)
+    ns64 = n_sets(nb64, dev)
+    sets = [(E64.clone(), R0[:T64].clone(), torch.empty_like(R0[:T64]),
+             torch.empty_like(R0[:T64])) for _ in range(ns64)]
+    for name, ready in (("moe_decode_t64", False), ("moe_decode_t64_routing_ready", True)):
+        ls = [(lambda s=s: lb.lb_moe_finalize_fold_norm(
+            s[0], T64 * w.topk, I64, W64, w.topk, s[1], s[2], G, s[3], None, None,
+            T64, w.H, w.eps, None, stream=sp, routing_ready=ready)) for s in sets]
+        el, _ = time_graph(ls, steps, 20, stream, dist)
+        record(name, T64, nb64, el, steps, plan_of(lb, T64, w.H, w.topk + 1, props),
+               f"rotated {ns64} sets")
+    del sets, ls
     # the headline call with the Gemma weight and an owned snapshot of residual'
     w = wl.prefill_fold_norm_fp8()
     nb = bytes_fold(w.K, w.T, w.H, fp8=True, y=False) + w.T * w.H * 2

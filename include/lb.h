@@ -90,6 +90,16 @@ int lb_version(void);
  * An extra contribution added exactly once ("add_to_output") is one more partial.
  */
 #define LB_OPT_GEMMA_WEIGHT 1u
+/*
+ * LB_OPT_ROUTING_READY (lb_moe_finalize_fold_norm only; other calls return
+ * LB_ERR_UNSUPPORTED): the caller promises that idx and w were complete before the
+ * kernel that immediately precedes this call on its stream began, as they are when the
+ * router runs ahead of the expert GEMMs.  The call then reads its first tokens' indices
+ * and weights without waiting for that kernel to finish (the call's kernels are
+ * programmatic dependents of it); every other read still waits.  Without the promise
+ * (default) nothing is read before the preceding kernel has finished.
+ */
+#define LB_OPT_ROUTING_READY 2u
 
 typedef struct {
     unsigned int flags;

@@ -207,11 +207,15 @@ lb_status check_stream_buffers(const void *residual_in, void *residual_out,
     return LB_OK;
 }
 
-// Options: known flags only; the snapshot is one more output of residual's shape.
-lb_status check_options(const lb_options *opt, int64_t rows, int64_t H, BufList *l) {
+// Options: known flags only (the routing promise on the MoE call alone); the snapshot
+// is one more output of residual's shape.
+lb_status check_options(const lb_options *opt, int64_t rows, int64_t H, BufList *l,
+                        bool moe = false) {
     if (opt == nullptr)
         return LB_OK;
-    if (opt->flags & ~static_cast<unsigned int>(LB_OPT_GEMMA_WEIGHT))
+    const unsigned int known =
+        LB_OPT_GEMMA_WEIGHT | (moe ? static_cast<unsigned int>(LB_OPT_ROUTING_READY) : 0u);
+    if (opt->flags & ~known)
         return LB_ERR_UNSUPPORTED;
     if (opt->residual_snapshot != nullptr) {
         LB_TRY(check_tensor(opt->residual_snapshot));
@@ -222,6 +226,7 @@ lb_status check_options(const lb_options *opt, int64_t rows, int64_t H, BufList 
 
 void set_options(lb::Params *p, const lb_options *opt) {
     p->gemma = (opt != nullptr && (opt->flags & LB_OPT_GEMMA_WEIGHT)) ? 1 : 0;
+    p->routing_ready = (opt != nullptr && (opt->flags & LB_OPT_ROUTING_READY)) ? 1 : 0;
     p->snapshot = opt != nullptr ? static_cast<uint16_t *>(opt->residual_snapshot) : nullptr;
 }
 
@@ -527,7 +532,7 @@ lb_status lb_moe_finalize_fold_norm(const void *expert_out, int64_t n_expert_row
     l.add(bad_index_flag, 4, true);
     LB_TRY(check_stream_buffers(residual_in, residual_out, gamma, y_out, q_out, scale_out, T,
                                 H, &l));
-    LB_TRY(check_options(options, T, H, &l));
+    LB_TRY(check_options(options, T, H, &l, true));
     LB_TRY(check_overlaps(l));
     lb::Params p;
     std::memset(&p, 0, sizeof p);

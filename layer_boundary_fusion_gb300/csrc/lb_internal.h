@@ -78,6 +78,7 @@ struct Params {
     const float *w;
     int topk;
     int32_t *bad_index;
+    int routing_ready;         // idx, w may be read before griddepcontrol.wait
     // residual stream and read
     const uint16_t *residual_in;
     uint16_t *residual_out;

@@ -46,6 +46,18 @@ __device__ __forceinline__ uint4 ld_once(const void *ptr) {
     return v;
 }
 
+// The same load under a predicate: no memory access (and zeros) when `pred` is false,
+// so that a run of data-dependent loads needs no branches between them.
+__device__ __forceinline__ uint4 ld_once_if(const void *ptr, bool pred) {
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    asm("{\n\t.reg .pred p;\n\t"
+        "setp.ne.u32 p, %5, 0;\n\t"
+        "@p ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];\n\t}"
+        : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w)
+        : "l"(ptr), "r"(static_cast<uint32_t>(pred)));
+    return v;
+}
+
 // The residual may be overwritten in place by this same kernel, so it is read
 // through the coherent path.
 __device__ __forceinline__ uint4 ld_residual(const void *ptr) {
@@ -254,7 +266,21 @@ __global__ void __launch_bounds__(512, 1) boundary_kernel(const __grid_constant_
     }
     const bool has_res = p.residual_in != nullptr;
     const bool need_read = kFp8 || p.y_out != nullptr;
-    pdl_wait();                                    // every global access comes after this
+    // MoE with the caller's promise that the routing was complete before the preceding
+    // kernel began: the first chunk's indices and weights are read before the wait
+    // (not by the four-vector variant, whose registers are full).
+    int32_t e_early[kChunk];
+    float w_early[kChunk];
+    const bool early_meta = kMode == kMoe && kVpt <= 2 && p.routing_ready;
+    if (early_meta) {
+#pragma unroll
+        for (int jj = 0; jj < kChunk; ++jj)
+            if (jj < p.topk) {
+                e_early[jj] = __ldg(p.idx + row * p.topk + jj);
+                w_early[jj] = __ldg(p.w + row * p.topk + jj);
+            }
+    }
+    pdl_wait();                                    // every other global access after this
 
     // Residual and gamma loads go out with the first chunk of partials.
     uint4 rv[kVpt];
@@ -331,27 +357,37 @@ __global__ void __launch_bounds__(512, 1) boundary_kernel(const __grid_constant_
         // rounded before its add)
         const int64_t tk = row * p.topk;
         for (int j0 = 0; j0 < p.topk; j0 += kChunk) {
-            uint4 buf[kChunk][kVpt];
+            // the chunk's routing first, then every expert-row load under a predicate
+            // (no branch between the loads), then the products in slot order
+            int32_t ev[kChunk];
             float wj[kChunk];
             bool ok[kChunk];
 #pragma unroll
             for (int jj = 0; jj < kChunk; ++jj) {
-                ok[jj] = false;
+                const bool in = j0 + jj < p.topk;
+                const bool pre = early_meta && j0 == 0;
+                ev[jj] = -1;
                 wj[jj] = 0.0f;
-                if (j0 + jj < p.topk) {
-                    const int32_t e = __ldg(p.idx + tk + j0 + jj);
-                    wj[jj] = __ldg(p.w + tk + j0 + jj);
-                    ok[jj] = (e >= 0) & (static_cast<int64_t>(e) < p.n_expert_rows);
-                    if (ok[jj]) {
-                        const uint16_t *src = p.expert_out + static_cast<int64_t>(e) * H;
-#pragma unroll
-                        for (int i = 0; i < kVpt; ++i)
-                            if (act[i])
-                                buf[jj][i] = ld_once(src + col[i]);
-                    } else if (p.bad_index != nullptr && threadIdx.x == 0 && crank == 0) {
-                        *p.bad_index = 1;
-                    }
+                if (in) {
+                    ev[jj] = pre ? e_early[jj] : __ldg(p.idx + tk + j0 + jj);
+                    wj[jj] = pre ? w_early[jj] : __ldg(p.w + tk + j0 + jj);
                 }
+            }
+            uint4 buf[kChunk][kVpt];
+#pragma unroll
+            for (int jj = 0; jj < kChunk; ++jj) {
+                ok[jj] = (ev[jj] >= 0) & (static_cast<int64_t>(ev[jj]) < p.n_expert_rows);
+                const uint16_t *src =
+                    p.expert_out + static_cast<int64_t>(ok[jj] ? ev[jj] : 0) * H;
+#pragma unroll
+                for (int i = 0; i < kVpt; ++i)
+                    buf[jj][i] = ld_once_if(src + col[i], ok[jj] && act[i]);
+            }
+            if (p.bad_index != nullptr && threadIdx.x == 0 && crank == 0) {
+#pragma unroll
+                for (int jj = 0; jj < kChunk; ++jj)
+                    if (j0 + jj < p.topk && !ok[jj])
+                        *p.bad_index = 1;
             }
 #pragma unroll
             for (int jj = 0; jj < kChunk; ++jj)

@@ -343,13 +343,14 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
         const int64_t H = p.H;
         const int64_t rows = p.rows;
         int64_t row = next_row(p, blockIdx.x);
-        pdl_wait();
         // MoE: lane j < topk fetches slot j's index and weight of a row into the row's
         // metadata block, one cp.async group per row, LB_MOE_META_AHEAD rows ahead of
         // its issue, so that no index load sits between a free stage and its copies
         // (the first rows' metadata is fetched at once).  Two rows ahead measured
         // faster than one (the load latency under a saturated memory system outlasts
-        // a row) and than a full ring of stages ahead.
+        // a row) and than a full ring of stages ahead.  With the caller's promise that
+        // the routing was complete before the preceding kernel began, the first rows'
+        // metadata is fetched before griddepcontrol.wait.
         int64_t ahead = row;             // next row whose metadata is fetched
         auto fetch_meta = [&](int blk) {
             if (kMode != kMoe)
@@ -363,8 +364,14 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
                 ahead = next_row(p, ahead + gridDim.x);
         };
         const int ahead_rows = ns < LB_MOE_META_AHEAD ? ns : LB_MOE_META_AHEAD;
-        for (int b = 0; b < ahead_rows; ++b)
-            fetch_meta(b);
+        const bool early_meta = kMode == kMoe && p.routing_ready;
+        if (early_meta)
+            for (int b = 0; b < ahead_rows; ++b)
+                fetch_meta(b);
+        pdl_wait();
+        if (!early_meta)
+            for (int b = 0; b < ahead_rows; ++b)
+                fetch_meta(b);
         // Who issues a stage's copies.  Lane 0 issuing them one after another keeps a
         // stage's bytes in order for copies of 6 KB and more (rows of 3072 elements and
         // up); for shorter slots the issue itself (about 0.15 us per copy from one

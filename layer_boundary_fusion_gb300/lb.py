@@ -34,6 +34,7 @@ LB_KERNEL_STREAM = 1
 LB_DEVICE_ERR_TIMEOUT = 1
 LB_DEVICE_ERR_LAUNCH = 2
 LB_OPT_GEMMA_WEIGHT = 1
+LB_OPT_ROUTING_READY = 2
 
 LB_RESIDUAL_INITIAL = 0
 LB_RESIDUAL_WRITTEN = 1
@@ -186,11 +187,12 @@ def _ptr_array(items: Sequence) -> ctypes.Array:
     return arr
 
 
-def _options(gemma: bool, residual_snapshot):
+def _options(gemma: bool, residual_snapshot, routing_ready: bool = False):
     """lb_options for the keyword arguments, or None (NULL) for the defaults."""
-    if not gemma and residual_snapshot is None:
+    if not gemma and residual_snapshot is None and not routing_ready:
         return None
-    return ctypes.byref(Options(LB_OPT_GEMMA_WEIGHT if gemma else 0, _ptr(residual_snapshot)))
+    flags = (LB_OPT_GEMMA_WEIGHT if gemma else 0) | (LB_OPT_ROUTING_READY if routing_ready else 0)
+    return ctypes.byref(Options(flags, _ptr(residual_snapshot)))
 
 
 def _check(status: int, func: str) -> None:
@@ -248,14 +250,14 @@ def lb_fold_norm_fp8(partials, residual_in, residual_out, gamma, q_out, scale_ou
 def lb_moe_finalize_fold_norm(expert_out, n_expert_rows, idx, w, topk, residual_in,
                               residual_out, gamma, y_out, q_out, scale_out, T, H, eps,
                               bad_index_flag=None, stream=None, *, gemma=False,
-                              residual_snapshot=None) -> None:
+                              residual_snapshot=None, routing_ready=False) -> None:
     lib = load()
     s = _stream(stream, expert_out, residual_out, y_out, q_out)
     _check(lib.lb_moe_finalize_fold_norm(_ptr(expert_out), n_expert_rows, _ptr(idx), _ptr(w),
                                          topk, _ptr(residual_in), _ptr(residual_out),
                                          _ptr(gamma), _ptr(y_out), _ptr(q_out),
                                          _ptr(scale_out), T, H, eps, _ptr(bad_index_flag),
-                                         _options(gemma, residual_snapshot), s),
+                                         _options(gemma, residual_snapshot, routing_ready), s),
            "lb_moe_finalize_fold_norm")
 
 

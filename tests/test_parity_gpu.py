@@ -174,7 +174,8 @@ def test_ragged_slice_every_rank(lb, fp8):
                              f"slice {r} fp8", rows=v)
 
 
-def _gpu_moe(lb, w, *, idx=None, residual=True, fp8=False, flag=False, want_y=True):
+def _gpu_moe(lb, w, *, idx=None, residual=True, fp8=False, flag=False, want_y=True,
+             routing_ready=False):
     T, H = w.T, w.H
     idx = w.idx if idx is None else idx
     E = dev_bits(w.expert_out)
@@ -190,7 +191,8 @@ def _gpu_moe(lb, w, *, idx=None, residual=True, fp8=False, flag=False, want_y=Tr
     before = _snapshot([E, I, Wt, R, G])
     lb.lb_moe_finalize_fold_norm(E, w.expert_out.shape[0], I, Wt, idx.shape[1], R, ro.t, G,
                                  yo.t if yo else None, qo.t if fp8 else None,
-                                 so.t if fp8 else None, T, H, w.eps, F)
+                                 so.t if fp8 else None, T, H, w.eps, F,
+                                 routing_ready=routing_ready)
     torch.cuda.synchronize()
     _assert_unchanged(before, [E, I, Wt, R, G])
     out = {"residual_out": ro}
@@ -302,6 +304,21 @@ def test_stream_modes_on_both_kernels(lb, T, H):
                         want_y_fp8=True), full, "in place fp8")
 
 
+@pytest.mark.parametrize("T", [64, 1024])             # row kernel, stream kernel
+@pytest.mark.parametrize("fp8", [False, True])
+def test_moe_routing_ready(lb, T, fp8):
+    """With the routing promise the MoE call reads its first tokens' routing early and
+    computes exactly what it computes without it."""
+    w = wl.moe_workload("ready", T, 4096, 64, 8, seed=44 + T)
+    want = oracle.moe_finalize_fold_norm(w.expert_out, w.idx, w.w, w.residual, w.gamma,
+                                         w.eps, want_fp8=fp8)
+    got = _gpu_moe(lb, w, fp8=fp8, routing_ready=True)
+    check_fold(got, want, f"moe routing ready T={T}")
+    plain = _gpu_moe(lb, w, fp8=fp8)
+    for k in got:
+        assert_bits_equal(got[k], plain[k], f"routing ready vs default: {k}")
+
+
 def test_moe_bad_index_on_the_stream_kernel(lb):
     w = wl.moe_workload("bad2", 400, 2048, 16, 4, seed=43)
     assert plan(lb, 400, 2048, 5).kernel == lb.LB_KERNEL_STREAM
@@ -315,12 +332,16 @@ def test_moe_bad_index_on_the_stream_kernel(lb):
     check_fold(got, want, "moe bad index, stream kernel")
 
 
-def test_dependent_chain_of_boundaries(lb):
+@pytest.mark.parametrize("routing_ready", [False, True])
+def test_dependent_chain_of_boundaries(lb, routing_ready):
     """Layers back to back on one stream with no host synchronisation: each boundary
     reads the residual the previous one wrote, and a torch kernel writes the next
     partials just before each call (the kernels are programmatic dependents of the
-    previous launch, so this checks that every read waits for its producer)."""
-    rows = (2048, 64, 700, 1024, 2048)           # stream, row, stream, MoE, stream kernels
+    previous launch, so this checks that every read waits for its producer).  With
+    routing_ready the MoE layers' routing is written before their expert rows, and the
+    calls are told so: the expert rows, written by the kernel just before each call,
+    must still be read after it."""
+    rows = (2048, 64, 700, 1024, 2048, 64)       # stream, row, stream, MoE, stream, MoE(row)
     H = 2048
     rng = np.random.default_rng(81)
     gamma = (1 + 0.1 * rng.standard_normal(H)).astype(np.float32)
@@ -330,6 +351,10 @@ def test_dependent_chain_of_boundaries(lb):
     want_res = res_host.copy()
     ys = []
     for li, T in enumerate(rows):
+        moe = li in (3, 5)                         # MoE finalize layers
+        if moe and routing_ready:                  # the router ran before the experts
+            idx = torch.arange(T * 3, dtype=torch.int32, device="cuda").view(T, 3)
+            wts = torch.full((T, 3), 1.0, dtype=torch.float32, device="cuda")
         seeds = [1000 * li + k for k in range(3)]
         P_host = [wl.to_bf16_bits(np.random.default_rng(sd).standard_normal((T, H))
                                   .astype(np.float32)) for sd in seeds]
@@ -338,12 +363,14 @@ def test_dependent_chain_of_boundaries(lb):
             d.view(torch.int16).copy_(torch.from_numpy(h.view(np.int16)).cuda() * 1)
         Rn = torch.empty_like(R)
         Y = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
-        if li == 3:                                # a MoE finalize layer
-            idx = torch.arange(T * 3, dtype=torch.int32, device="cuda").view(T, 3)
+        if moe:
+            if not routing_ready:
+                idx = torch.arange(T * 3, dtype=torch.int32, device="cuda").view(T, 3)
             E = torch.cat(P, dim=1).view(T * 3, H)
-            wts = torch.full((T, 3), 1.0, dtype=torch.float32, device="cuda")
+            if not routing_ready:
+                wts = torch.full((T, 3), 1.0, dtype=torch.float32, device="cuda")
             lb.lb_moe_finalize_fold_norm(E, T * 3, idx, wts, 3, R[:T], Rn[:T], G, Y, None,
-                                         None, T, H, 1e-6)
+                                         None, T, H, 1e-6, routing_ready=routing_ready)
             Eh = np.stack(P_host, axis=1).reshape(T * 3, H)
             o = oracle.moe_finalize_fold_norm(Eh, np.arange(T * 3, dtype=np.int32)
                                               .reshape(T, 3), np.ones((T, 3), np.float32),
