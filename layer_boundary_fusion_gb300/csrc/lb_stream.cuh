@@ -372,11 +372,12 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
         if (!early_meta)
             for (int b = 0; b < ahead_rows; ++b)
                 fetch_meta(b);
-        // Who issues a stage's copies.  Lane 0 issuing them one after another keeps a
-        // stage's bytes in order for copies of 6 KB and more (rows of 3072 elements and
-        // up); for shorter slots the issue itself (about 0.15 us per copy from one
-        // lane) bounds the kernel, and each lane issues its own slot's copy.
-        const bool lane_issue = slot_bytes <= LB_STREAM_LANE_ISSUE_BYTES;
+        // Who issues a stage's copies.  Lane 0 issuing them one after another measured
+        // best for the fold's copies of 6 KB and more (rows of 3072 elements and up);
+        // for shorter slots the issue itself (about 0.15 us per copy from one lane)
+        // bounds the kernel, and each lane issues its own slot's copy, as it does for
+        // the gathered expert rows of a MoE finalize at any size.
+        const bool lane_issue = kMode == kMoe || slot_bytes <= LB_STREAM_LANE_ISSUE_BYTES;
         int s = 0;                       // stage of the next chunk to issue
         uint32_t k = 0;                  // use of that stage
         int units = 0;                   // chunks issued (one per row unless chunked)
