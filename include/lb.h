@@ -127,7 +127,7 @@ typedef struct {
  * The launch the library makes for `rows` rows of width H, each reading `n_inputs`
  * input rows (K partials or topk expert rows, plus one if there is a residual), on a
  * GPU with `num_sms` SMs and `smem_per_block` bytes of opt-in shared memory per CTA.
- * Host-only, pure.  Calls with at least one row per SM stream through the
+ * Host-only, pure.  Calls with more rows than SMs stream through the
  * persistent TMA kernel when a double-buffered stage fits (a stage holds a whole row
  * of every input, or for rows of more than 8192 elements, up to 16384, one of 2-4
  * column chunks of it); smaller calls use the row kernel, one CTA per row, splitting

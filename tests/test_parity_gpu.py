@@ -281,7 +281,7 @@ def test_stream_modes_on_both_kernels(lb, T, H):
     """The same stream modes with enough rows for the persistent TMA kernel (T=700;
     T=300 with rows in column chunks) and few enough for the row kernel (T=50)."""
     w = wl.fold_workload("modes2", 3, T, H, seed=52 + T)
-    kernel = lb.LB_KERNEL_STREAM if T >= torch.cuda.get_device_properties(0) \
+    kernel = lb.LB_KERNEL_STREAM if T > torch.cuda.get_device_properties(0) \
         .multi_processor_count else lb.LB_KERNEL_ROW
     assert plan(lb, T, H, 4).kernel == kernel
     full = oracle.fold_norm(w.partials, w.residual, w.gamma, w.eps, want_fp8=True)
@@ -413,7 +413,8 @@ def test_specified_workloads_take_the_intended_kernels(lb):
     (1, 4, 32768),      # four vectors per thread, a row split over a 2-CTA cluster
     (5, 301, 4096),     # K above one load chunk, ragged last wave
     (4, 2048, 1024),    # row kernel past the SM count (rows of <= 1024 elements)
-    (8, 152, 2048),     # stream kernel, one vector per thread, a copy per producer lane
+    (8, 152, 2048),     # row kernel: one row per SM
+    (8, 153, 2048),     # stream kernel, one vector per thread, a copy per producer lane
     (2, 160, 4096),     # stream kernel, one or two rows per CTA
     (4, 1000, 4096),    # stream kernel
     (16, 300, 1024),    # row kernel at the maximum K, past the SM count
