@@ -228,7 +228,8 @@ def test_moe_finalize_fp8_and_initial(lb):
                                         (1, 2048, 128, 8),
                                         (300, 8192, 64, 8),     # row kernel past the SMs
                                         (200, 12288, 16, 4),    # stream kernel, 3 chunks
-                                        (160, 10240, 32, 8)])   # 3 chunks, the last short
+                                        (160, 10240, 32, 8),    # 3 chunks, the last short
+                                        (1200, 12288, 64, 2)])  # chunked, many wraps
 def test_moe_shapes(lb, T, H, E, topk):
     w = wl.moe_workload("m", T, H, E, topk, seed=T + H)
     want = oracle.moe_finalize_fold_norm(w.expert_out, w.idx, w.w, w.residual, w.gamma, w.eps)
@@ -436,6 +437,7 @@ def test_specified_workloads_take_the_intended_kernels(lb):
     (8, 200, 8192),     # row kernel: whole rows of 9 inputs do not double-buffer
     (16, 153, 8200),    # stream kernel, maximum K, 4 chunks of 10 warps, 65 vectors in the last
     (8, 160, 12288),    # stream kernel, 3 chunks of 16 warps, 2 stages
+    (2, 1500, 10240),   # stream kernel, chunked rows: ~10 rows per CTA, the ring wraps often
 ])
 def test_shapes(lb, K, T, H):
     w = wl.fold_workload("shape", K, T, H, seed=K * 1000 + T + H)
