@@ -56,6 +56,7 @@ typedef struct CUstream_st *lb_stream_t;
 #define LB_MAX_TOPK 16    /* routed experts per token in the MoE finalize */
 #define LB_MAX_SETS 64    /* token sets in a ragged batch */
 #define LB_MAX_H 131072   /* hidden size */
+#define LB_MAX_ROWS 134217728 /* rows of one call (2^27: every launch grid fits) */
 
 typedef enum {
     LB_OK = 0,
@@ -161,7 +162,8 @@ lb_status lb_device_error(unsigned int *flags, int clear);
  *   residual_out bf16 [T,H] receives bf16(o), or NULL to skip (read-only boundary)
  *   gamma        float32 [H]; required when y_out is given
  *   y_out        bf16 [T,H] receives the RMSNorm read, or NULL for no read
- *   T, H         rows and hidden size; T >= 0, 8 <= H <= LB_MAX_H, H % 8 == 0
+ *   T, H         rows and hidden size; 0 <= T <= LB_MAX_ROWS, 8 <= H <= LB_MAX_H,
+ *                H % 8 == 0 (LB_ERR_UNSUPPORTED outside these ranges)
  *   eps          >= 0 and finite
  *
  * The stream operations of the Residual stream section map to argument patterns:

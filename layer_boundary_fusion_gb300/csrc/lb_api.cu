@@ -65,7 +65,7 @@ lb_status check_shape(int64_t T, int64_t H, float eps) {
         return LB_ERR_INVALID_ARGUMENT;
     if (H % 8 != 0 || H > LB_MAX_H)
         return LB_ERR_UNSUPPORTED;
-    if (T > (int64_t(1) << 27))          // grid: rows x 8 CTAs must fit in 2^31 - 1
+    if (T > LB_MAX_ROWS)                 // grid: rows x 8 CTAs must fit in 2^31 - 1
         return LB_ERR_UNSUPPORTED;
     return LB_OK;
 }

@@ -28,6 +28,7 @@ LB_MAX_K = 16
 LB_MAX_TOPK = 16
 LB_MAX_SETS = 64
 LB_MAX_H = 131072
+LB_MAX_ROWS = 1 << 27
 
 LB_KERNEL_ROW = 0
 LB_KERNEL_STREAM = 1

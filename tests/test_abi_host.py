@@ -63,7 +63,7 @@ def test_status_strings_and_version(lib):
 
 def test_header_constants_match_binding(lib):
     text = open(os.path.join(ROOT, "include", "lb.h")).read()
-    for name in ("LB_MAX_K", "LB_MAX_TOPK", "LB_MAX_SETS", "LB_MAX_H"):
+    for name in ("LB_MAX_K", "LB_MAX_TOPK", "LB_MAX_SETS", "LB_MAX_H", "LB_MAX_ROWS"):
         m = re.search(rf"#define {name} (\d+)", text)
         assert int(m.group(1)) == getattr(lib, name)
 
@@ -177,6 +177,7 @@ run("H_not_multiple_of_8", f, P, a(2), a(3), a(4), a(5), T, 60, 1e-6, 0)
 run("H_zero", f, P, a(2), a(3), a(4), a(5), T, 0, 1e-6, 0)
 run("H_too_big", f, P, a(2), a(3), a(4), a(5), T, lb.LB_MAX_H + 8, 1e-6, 0)
 run("T_negative", f, P, a(2), a(3), a(4), a(5), -1, H, 1e-6, 0)
+run("T_too_big", f, P, a(2), a(3), a(4), a(5), lb.LB_MAX_ROWS + 1, H, 1e-6, 0)
 run("eps_negative", f, P, a(2), a(3), a(4), a(5), T, H, -1e-6, 0)
 run("eps_nan", f, P, a(2), a(3), a(4), a(5), T, H, float("nan"), 0)
 run("y_misaligned", f, P, a(2), a(3), a(4), a(5) + 2, T, H, 1e-6, 0)
@@ -241,7 +242,7 @@ EXPECTED = {
     "ok_empty": 0, "K_negative": 1, "K_too_big": 3, "partial_null": 1,
     "partial_misaligned": 2, "K0_no_residual": 1, "nothing_to_write": 1,
     "y_without_gamma": 1, "H_not_multiple_of_8": 3, "H_zero": 1, "H_too_big": 3,
-    "T_negative": 1, "eps_negative": 1, "eps_nan": 1, "y_misaligned": 2,
+    "T_negative": 1, "T_too_big": 3, "eps_negative": 1, "eps_nan": 1, "y_misaligned": 2,
     "gamma_misaligned": 2, "y_overlaps_partial": 1, "y_overlaps_residual_out": 1,
     "residual_out_shifted_over_in": 1, "in_place_empty_ok": 0,
     "empty_null_buffers_ok": 0, "empty_bad_H": 3, "empty_K_too_big": 3,
