@@ -333,6 +333,16 @@ def measure_variants(lb, dev, stream, dist, steps):
         record(name + "_hot_l2", w.T, nb, el, steps,
                plan_of(lb, w.T, w.H, w.K + (w.residual is not None), props),
                "hot: one buffer set, L2-resident")
+        # with the residual promise (LB_OPT_RESIDUAL_READY: no call here writes a
+        # residual or gamma that the next call reads): residual and gamma load while
+        # the previous call drains
+        ls = [(lambda s=s: lb.lb_fold_norm(s.P, s.R, s.ro, s.G, s.yo, w.T, w.H, w.eps,
+                                           stream=stream.cuda_stream, residual_ready=True))
+              for s in sets]
+        el, _ = time_graph(ls, steps, 20, stream, dist)
+        record(name + "_residual_ready", w.T, nb, el, steps,
+               plan_of(lb, w.T, w.H, w.K + (w.residual is not None), props),
+               f"rotated {ns} sets")
         del sets, ls
     # ragged row slice r=3 of 8
     w = wl.ragged_slice()
@@ -439,10 +449,13 @@ def measure_variants(lb, dev, stream, dist, steps):
     ns64 = n_sets(nb64, dev)
     sets = [(E64.clone(), R0[:T64].clone(), torch.empty_like(R0[:T64]),
              torch.empty_like(R0[:T64])) for _ in range(ns64)]
-    for name, ready in (("moe_decode_t64", False), ("moe_decode_t64_routing_ready", True)):
+    for name, ready, res_ready in (("moe_decode_t64", False, False),
+                                   ("moe_decode_t64_routing_ready", True, False),
+                                   ("moe_decode_t64_both_promises", True, True)):
         ls = [(lambda s=s: lb.lb_moe_finalize_fold_norm(
             s[0], T64 * w.topk, I64, W64, w.topk, s[1], s[2], G, s[3], None, None,
-            T64, w.H, w.eps, None, stream=sp, routing_ready=ready)) for s in sets]
+            T64, w.H, w.eps, None, stream=sp, routing_ready=ready,
+            residual_ready=res_ready)) for s in sets]
         el, _ = time_graph(ls, steps, 20, stream, dist)
         record(name, T64, nb64, el, steps, plan_of(lb, T64, w.H, w.topk + 1, props),
                f"rotated {ns64} sets")

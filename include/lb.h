@@ -101,6 +101,14 @@ int lb_version(void);
  * (default) nothing is read before the preceding kernel has finished.
  */
 #define LB_OPT_ROUTING_READY 2u
+/*
+ * LB_OPT_RESIDUAL_READY (every call): the caller promises that residual_in and gamma
+ * were complete before the kernel that immediately precedes this call on its stream
+ * began, as they are between two layer boundaries (GEMMs run in between; gamma is a
+ * weight).  The call may then read them without waiting for that kernel to finish.
+ * The partials (or expert rows) and every output still wait for it.
+ */
+#define LB_OPT_RESIDUAL_READY 4u
 
 typedef struct {
     unsigned int flags;

@@ -213,8 +213,8 @@ lb_status check_options(const lb_options *opt, int64_t rows, int64_t H, BufList 
                         bool moe = false) {
     if (opt == nullptr)
         return LB_OK;
-    const unsigned int known =
-        LB_OPT_GEMMA_WEIGHT | (moe ? static_cast<unsigned int>(LB_OPT_ROUTING_READY) : 0u);
+    const unsigned int known = LB_OPT_GEMMA_WEIGHT | LB_OPT_RESIDUAL_READY |
+                               (moe ? static_cast<unsigned int>(LB_OPT_ROUTING_READY) : 0u);
     if (opt->flags & ~known)
         return LB_ERR_UNSUPPORTED;
     if (opt->residual_snapshot != nullptr) {
@@ -227,6 +227,7 @@ lb_status check_options(const lb_options *opt, int64_t rows, int64_t H, BufList 
 void set_options(lb::Params *p, const lb_options *opt) {
     p->gemma = (opt != nullptr && (opt->flags & LB_OPT_GEMMA_WEIGHT)) ? 1 : 0;
     p->routing_ready = (opt != nullptr && (opt->flags & LB_OPT_ROUTING_READY)) ? 1 : 0;
+    p->residual_ready = (opt != nullptr && (opt->flags & LB_OPT_RESIDUAL_READY)) ? 1 : 0;
     p->snapshot = opt != nullptr ? static_cast<uint16_t *>(opt->residual_snapshot) : nullptr;
 }
 

@@ -79,6 +79,7 @@ struct Params {
     int topk;
     int32_t *bad_index;
     int routing_ready;         // idx, w may be read before griddepcontrol.wait
+    int residual_ready;        // residual_in, gamma may be read before it
     // residual stream and read
     const uint16_t *residual_in;
     uint16_t *residual_out;

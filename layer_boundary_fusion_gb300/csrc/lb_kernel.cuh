@@ -280,7 +280,12 @@ __global__ void __launch_bounds__(512, 1) boundary_kernel(const __grid_constant_
                 w_early[jj] = __ldg(p.w + row * p.topk + jj);
             }
     }
-    pdl_wait();                                    // every other global access after this
+    // Every global access after griddepcontrol.wait, but for what the caller promised
+    // was complete before the previous kernel began: the routing above, and with
+    // residual_ready the residual and gamma, which then load while that kernel drains.
+    const bool early_res = p.residual_ready != 0;
+    if (!early_res)
+        pdl_wait();
 
     // Residual and gamma loads go out with the first chunk of partials.
     uint4 rv[kVpt];
@@ -311,6 +316,9 @@ __global__ void __launch_bounds__(512, 1) boundary_kernel(const __grid_constant_
                 gm[i][e] = make_float2(0.0f, 0.0f);
         }
     }
+
+    if (early_res)
+        pdl_wait();
 
     // o in binary32 pairs, summed in the definition's order (mixed-precision and packed
     // adds round each element like the scalar binary32 add)

@@ -487,7 +487,11 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
         // chunked rows: vector i is vector ct of chunk i
         soff[i] = static_cast<uint32_t>((kChunked ? ct : v) * 16);
     }
-    pdl_wait();
+    // gamma before griddepcontrol.wait only on the caller's promise that it was complete
+    // before the previous kernel began
+    const bool early_gamma = p.residual_ready != 0;
+    if (!early_gamma)
+        pdl_wait();
 #pragma unroll
     for (int i = 0; i < kVpt; ++i) {
         if (act[i] && need_read) {
@@ -512,6 +516,8 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
                 gm[i][e] = make_float2(0.0f, 0.0f);
         }
     }
+    if (early_gamma)
+        pdl_wait();
     // the weight of vector v's elements 2e, 2e + 1
     auto weight = [&](int v, int e) -> float2 {
         if (!kChunked)

@@ -36,6 +36,7 @@ LB_DEVICE_ERR_TIMEOUT = 1
 LB_DEVICE_ERR_LAUNCH = 2
 LB_OPT_GEMMA_WEIGHT = 1
 LB_OPT_ROUTING_READY = 2
+LB_OPT_RESIDUAL_READY = 4
 
 LB_RESIDUAL_INITIAL = 0
 LB_RESIDUAL_WRITTEN = 1
@@ -188,11 +189,13 @@ def _ptr_array(items: Sequence) -> ctypes.Array:
     return arr
 
 
-def _options(gemma: bool, residual_snapshot, routing_ready: bool = False):
+def _options(gemma: bool, residual_snapshot, routing_ready: bool = False,
+             residual_ready: bool = False):
     """lb_options for the keyword arguments, or None (NULL) for the defaults."""
-    if not gemma and residual_snapshot is None and not routing_ready:
+    if not gemma and residual_snapshot is None and not routing_ready and not residual_ready:
         return None
-    flags = (LB_OPT_GEMMA_WEIGHT if gemma else 0) | (LB_OPT_ROUTING_READY if routing_ready else 0)
+    flags = ((LB_OPT_GEMMA_WEIGHT if gemma else 0) | (LB_OPT_ROUTING_READY if routing_ready else 0)
+             | (LB_OPT_RESIDUAL_READY if residual_ready else 0))
     return ctypes.byref(Options(flags, _ptr(residual_snapshot)))
 
 
@@ -226,39 +229,42 @@ def lb_device_error(clear: bool = True) -> int:
 
 
 def lb_fold_norm(partials, residual_in, residual_out, gamma, y_out, T, H, eps,
-                 stream=None, *, gemma=False, residual_snapshot=None) -> None:
+                 stream=None, *, gemma=False, residual_snapshot=None,
+                 residual_ready=False) -> None:
     lib = load()
     partials = list(partials)
     s = _stream(stream, *partials, residual_in, residual_out, y_out)
     _check(lib.lb_fold_norm(_ptr_array(partials), len(partials), _ptr(residual_in),
                             _ptr(residual_out), _ptr(gamma), _ptr(y_out), T, H, eps,
-                            _options(gemma, residual_snapshot), s),
+                            _options(gemma, residual_snapshot, False, residual_ready), s),
            "lb_fold_norm")
 
 
 def lb_fold_norm_fp8(partials, residual_in, residual_out, gamma, q_out, scale_out, y_out,
-                     T, H, eps, stream=None, *, gemma=False, residual_snapshot=None) -> None:
+                     T, H, eps, stream=None, *, gemma=False, residual_snapshot=None,
+                     residual_ready=False) -> None:
     lib = load()
     partials = list(partials)
     s = _stream(stream, *partials, residual_in, residual_out, q_out)
     _check(lib.lb_fold_norm_fp8(_ptr_array(partials), len(partials), _ptr(residual_in),
                                 _ptr(residual_out), _ptr(gamma), _ptr(q_out),
                                 _ptr(scale_out), _ptr(y_out), T, H, eps,
-                                _options(gemma, residual_snapshot), s),
+                                _options(gemma, residual_snapshot, False, residual_ready), s),
            "lb_fold_norm_fp8")
 
 
 def lb_moe_finalize_fold_norm(expert_out, n_expert_rows, idx, w, topk, residual_in,
                               residual_out, gamma, y_out, q_out, scale_out, T, H, eps,
                               bad_index_flag=None, stream=None, *, gemma=False,
-                              residual_snapshot=None, routing_ready=False) -> None:
+                              residual_snapshot=None, routing_ready=False,
+                              residual_ready=False) -> None:
     lib = load()
     s = _stream(stream, expert_out, residual_out, y_out, q_out)
     _check(lib.lb_moe_finalize_fold_norm(_ptr(expert_out), n_expert_rows, _ptr(idx), _ptr(w),
                                          topk, _ptr(residual_in), _ptr(residual_out),
                                          _ptr(gamma), _ptr(y_out), _ptr(q_out),
                                          _ptr(scale_out), T, H, eps, _ptr(bad_index_flag),
-                                         _options(gemma, residual_snapshot, routing_ready), s),
+                                         _options(gemma, residual_snapshot, routing_ready, residual_ready), s),
            "lb_moe_finalize_fold_norm")
 
 
@@ -269,7 +275,8 @@ def _int32_array(values):
 
 def lb_slice_fold_norm(partials, T_pad, num_slices, slice_, set_offsets, set_counts,
                        residual_in, residual_out, gamma, y_out, q_out, scale_out, H, eps,
-                       stream=None, *, gemma=False, residual_snapshot=None) -> None:
+                       stream=None, *, gemma=False, residual_snapshot=None,
+                       residual_ready=False) -> None:
     lib = load()
     partials = list(partials)
     if len(set_offsets) != len(set_counts):
@@ -281,13 +288,14 @@ def lb_slice_fold_norm(partials, T_pad, num_slices, slice_, set_offsets, set_cou
                                   slice_, ctypes.cast(offs, _vp), ctypes.cast(cnts, _vp), n,
                                   _ptr(residual_in), _ptr(residual_out), _ptr(gamma),
                                   _ptr(y_out), _ptr(q_out), _ptr(scale_out), H, eps,
-                                  _options(gemma, residual_snapshot), s),
+                                  _options(gemma, residual_snapshot, False, residual_ready), s),
            "lb_slice_fold_norm")
 
 
 def lb_slice_fold_norm_v(partials, T_pad, set_, set_offsets, set_counts, residual_in,
                          residual_out, gamma, y_out, q_out, scale_out, H, eps, stream=None, *,
-                         gemma=False, residual_snapshot=None) -> None:
+                         gemma=False, residual_snapshot=None,
+                         residual_ready=False) -> None:
     lib = load()
     partials = list(partials)
     if len(set_offsets) != len(set_counts):
@@ -299,7 +307,7 @@ def lb_slice_fold_norm_v(partials, T_pad, set_, set_offsets, set_counts, residua
                                     ctypes.cast(offs, _vp), ctypes.cast(cnts, _vp), n,
                                     _ptr(residual_in), _ptr(residual_out), _ptr(gamma),
                                     _ptr(y_out), _ptr(q_out), _ptr(scale_out), H, eps,
-                                    _options(gemma, residual_snapshot), s),
+                                    _options(gemma, residual_snapshot, False, residual_ready), s),
            "lb_slice_fold_norm_v")
 
 
@@ -336,11 +344,12 @@ def lb_residual_leave_moe(s: ResidualStream, h: int, expert_out, n_expert_rows, 
 
 
 def lb_residual_prepare(s: ResidualStream, h: int, gamma, y_out, q_out, scale_out, eps,
-                        stream=None, *, gemma=False, residual_snapshot=None) -> int:
+                        stream=None, *, gemma=False, residual_snapshot=None,
+                        residual_ready=False) -> int:
     st = _stream(stream, gamma, y_out, q_out)
     return _handle("lb_residual_prepare", lambda o: load().lb_residual_prepare(
         ctypes.byref(s), h, _ptr(gamma), _ptr(y_out), _ptr(q_out), _ptr(scale_out), eps,
-        _options(gemma, residual_snapshot), st, o))
+        _options(gemma, residual_snapshot, False, residual_ready), st, o))
 
 
 def lb_residual_complete_output(s: ResidualStream, h: int, sum_out, stream=None) -> int:
@@ -375,8 +384,9 @@ def lb_residual_take_output(s: ResidualStream, h: int) -> int:
 
 
 def lb_residual_norm(s: ResidualStream, h: int, gamma, y_out, q_out, scale_out, eps,
-                     stream=None, *, gemma=False, residual_snapshot=None) -> None:
+                     stream=None, *, gemma=False, residual_snapshot=None,
+                     residual_ready=False) -> None:
     st = _stream(stream, gamma, y_out, q_out)
     _check(load().lb_residual_norm(ctypes.byref(s), h, _ptr(gamma), _ptr(y_out), _ptr(q_out),
-                                   _ptr(scale_out), eps, _options(gemma, residual_snapshot),
+                                   _ptr(scale_out), eps, _options(gemma, residual_snapshot, False, residual_ready),
                                    st), "lb_residual_norm")

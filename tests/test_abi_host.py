@@ -210,10 +210,13 @@ run("moe_flag_in_experts", m, a(0), 32, a(1), a(8), 8, a(2), a(3), a(4), a(5), N
 # the routing promise: accepted by the MoE call (which then fails only for want of a
 # device), refused by the others
 run("moe_routing_ready_valid", lambda: m(a(0), 32, a(1), a(8), 8, a(2), a(3), a(4), a(5), None, None, T, H, 1e-6, None, 0, routing_ready=True))
-mo = lb.Options(4, None)
+mo = lb.Options(8, None)
 results["moe_unknown_flag"] = L.lb_moe_finalize_fold_norm(a(0), 32, a(1), a(8), 8, a(2), a(3), a(4), a(5), None, None, T, H, 1e-6, None, lb.ctypes.byref(mo), None)
 ro = lb.Options(lb.LB_OPT_ROUTING_READY, None)
 results["fold_routing_ready"] = L.lb_fold_norm((lb._vp * 2)(a(0), a(1)), 2, a(2), a(3), a(4), a(5), T, H, 1e-6, lb.ctypes.byref(ro), None)
+# the residual promise: accepted by every call
+run("fold_residual_ready_valid", lambda: f(P, a(2), a(3), a(4), a(5), T, H, 1e-6, 0, residual_ready=True))
+run("moe_both_promises_valid", lambda: m(a(0), 32, a(1), a(8), 8, a(2), a(3), a(4), a(5), None, None, T, H, 1e-6, None, 0, routing_ready=True, residual_ready=True))
 s = lb.lb_slice_fold_norm
 off, cnt = [0, 40, 552, 560], [37, 512, 5, 1470]
 run("slice_empty_ok", s, P, 0, 8, 0, off[:0], cnt[:0], a(2), a(3), a(4), a(5), None, None, H, 1e-6, 0)
@@ -252,6 +255,7 @@ EXPECTED = {
     "moe_no_experts": 1, "moe_rows_negative": 1, "moe_idx_misaligned": 2,
     "moe_half_fp8": 1, "moe_flag_in_experts": 1,
     "moe_routing_ready_valid": 4, "moe_unknown_flag": 3, "fold_routing_ready": 3,
+    "fold_residual_ready_valid": 4, "moe_both_promises_valid": 4,
     "slice_empty_ok": 0, "slice_uneven": 1, "slice_index_high": 1,
     "slice_index_negative": 1, "slice_zero_slices": 1, "slice_sets_overlap": 1,
     "slice_sets_descending": 1, "slice_set_past_end": 1, "slice_count_negative": 1,

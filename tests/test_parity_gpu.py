@@ -320,6 +320,21 @@ def test_moe_routing_ready(lb, T, fp8):
         assert_bits_equal(got[k], plain[k], f"routing ready vs default: {k}")
 
 
+@pytest.mark.parametrize("T,H", [(64, 4096), (300, 4096), (300, 12288)])  # row, stream, chunked
+@pytest.mark.parametrize("fp8", [False, True])
+def test_residual_ready(lb, T, H, fp8):
+    """With the residual promise the call loads residual and gamma early and computes
+    exactly what it computes without it (Gemma weight included)."""
+    w = wl.fold_workload("res_ready", 4, T, H, seed=45 + T + H)
+    want = oracle.fold_norm(w.partials, w.residual, w.gamma, w.eps, want_fp8=True,
+                            gemma=True)
+    got = _options_fold(lb, w, fp8=fp8, gemma=True, snapshot=False, residual_ready=True)
+    check_fold(got, want, f"residual ready T={T} H={H}")
+    plain = _options_fold(lb, w, fp8=fp8, gemma=True, snapshot=False)
+    for k in got:
+        assert_bits_equal(got[k], plain[k], f"residual ready vs default: {k}")
+
+
 def test_moe_bad_index_on_the_stream_kernel(lb):
     w = wl.moe_workload("bad2", 400, 2048, 16, 4, seed=43)
     assert plan(lb, 400, 2048, 5).kernel == lb.LB_KERNEL_STREAM
@@ -333,15 +348,18 @@ def test_moe_bad_index_on_the_stream_kernel(lb):
     check_fold(got, want, "moe bad index, stream kernel")
 
 
-@pytest.mark.parametrize("routing_ready", [False, True])
-def test_dependent_chain_of_boundaries(lb, routing_ready):
+@pytest.mark.parametrize("promises", [False, True])
+def test_dependent_chain_of_boundaries(lb, promises):
     """Layers back to back on one stream with no host synchronisation: each boundary
     reads the residual the previous one wrote, and a torch kernel writes the next
     partials just before each call (the kernels are programmatic dependents of the
     previous launch, so this checks that every read waits for its producer).  With
-    routing_ready the MoE layers' routing is written before their expert rows, and the
-    calls are told so: the expert rows, written by the kernel just before each call,
-    must still be read after it."""
+    promises the MoE layers' routing is written before their expert rows and every call
+    is told that its routing, residual and gamma were complete before the kernel just
+    before it began (true here: torch writes the partials after the residual's
+    producer has finished): the partials and expert rows, written by that kernel, must
+    still be read after it."""
+    routing_ready = promises
     rows = (2048, 64, 700, 1024, 2048, 64)       # stream, row, stream, MoE, stream, MoE(row)
     H = 2048
     rng = np.random.default_rng(81)
@@ -371,13 +389,14 @@ def test_dependent_chain_of_boundaries(lb, routing_ready):
             if not routing_ready:
                 wts = torch.full((T, 3), 1.0, dtype=torch.float32, device="cuda")
             lb.lb_moe_finalize_fold_norm(E, T * 3, idx, wts, 3, R[:T], Rn[:T], G, Y, None,
-                                         None, T, H, 1e-6, routing_ready=routing_ready)
+                                         None, T, H, 1e-6, routing_ready=promises,
+                                         residual_ready=promises)
             Eh = np.stack(P_host, axis=1).reshape(T * 3, H)
             o = oracle.moe_finalize_fold_norm(Eh, np.arange(T * 3, dtype=np.int32)
                                               .reshape(T, 3), np.ones((T, 3), np.float32),
                                               want_res[:T], gamma, 1e-6)
         else:
-            lb.lb_fold_norm(P, R[:T], Rn[:T], G, Y, T, H, 1e-6)
+            lb.lb_fold_norm(P, R[:T], Rn[:T], G, Y, T, H, 1e-6, residual_ready=promises)
             o = oracle.fold_norm(P_host, want_res[:T], gamma, 1e-6)
         Rn[T:] = R[T:]
         R = Rn
@@ -497,7 +516,7 @@ def test_runs_on_a_side_stream(lb):
 # Gemma weight (1 + gamma), residual snapshot, variable-size reduce-scatter (rsv)
 # --------------------------------------------------------------------------------------
 
-def _options_fold(lb, w, *, fp8, gemma, snapshot):
+def _options_fold(lb, w, *, fp8, gemma, snapshot, residual_ready=False):
     T, H = w.T, w.H
     P = [dev_bits(p) for p in w.partials]
     R = dev_bits(w.residual)
@@ -506,7 +525,8 @@ def _options_fold(lb, w, *, fp8, gemma, snapshot):
     sn = Guarded(T, H, torch.bfloat16) if snapshot else None
     qo = Guarded(T, H, torch.uint8) if fp8 else None
     so = Guarded(T, 0, torch.float32) if fp8 else None
-    kw = dict(gemma=gemma, residual_snapshot=sn.t if sn else None)
+    kw = dict(gemma=gemma, residual_snapshot=sn.t if sn else None,
+              residual_ready=residual_ready)
     if fp8:
         lb.lb_fold_norm_fp8(P, R, ro.t, G, qo.t, so.t, yo.t, T, H, w.eps, **kw)
     else:
