@@ -365,6 +365,14 @@ def measure_variants(lb, dev, stream, dist, steps):
     el, _ = time_graph(ls, steps, 20, stream, dist)
     record("ragged_slice", v, nb, el, steps, plan_of(lb, S, w.H, w.K + 1, props),
            f"rotated {ns} sets")
+    # with the residual promise: the first rows' residual copies go out early
+    ls = [(lambda s=s: lb.lb_slice_fold_norm(s[0], w.T_pad, w.num_slices, w.slice,
+                                            w.set_offsets, w.set_counts, s[1], s[2], G, s[3],
+                                            None, None, w.H, w.eps, stream=sp,
+                                            residual_ready=True)) for s in sets]
+    el, _ = time_graph(ls, steps, 20, stream, dist)
+    record("ragged_slice_residual_ready", v, nb, el, steps,
+           plan_of(lb, S, w.H, w.K + 1, props), f"rotated {ns} sets")
     # the same slice with the FP8 read
     nb8 = bytes_fold(w.K, v, w.H, y=False, fp8=True)
     Q = [(torch.empty((S, w.H), dtype=torch.uint8, device=dev),
@@ -472,6 +480,14 @@ def measure_variants(lb, dev, stream, dist, steps):
                                           residual_snapshot=s.snap)) for s in sets]
     el, _ = time_graph(ls, steps, 20, stream, dist)
     record("prefill_fp8_gemma_snapshot", w.T, nb, el, steps,
+           plan_of(lb, w.T, w.H, w.K + 1, props), f"rotated {ns} sets")
+    # the headline call with the residual promise
+    nb = bytes_fold(w.K, w.T, w.H, fp8=True, y=False)
+    ls = [(lambda s=s: lb.lb_fold_norm_fp8(s.P, s.R, s.ro, s.G, s.qo, s.so, None, w.T, w.H,
+                                          w.eps, stream=sp, residual_ready=True))
+          for s in sets]
+    el, _ = time_graph(ls, steps, 20, stream, dist)
+    record("prefill_fp8_residual_ready", w.T, nb, el, steps,
            plan_of(lb, w.T, w.H, w.K + 1, props), f"rotated {ns} sets")
     del sets, ls
     # fusion gain: the same fold + bf16 read as one fused call and as the unfused

@@ -66,6 +66,14 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
+// Post bytes that the current phase must also receive, without arriving: the phase
+// still completes only at the (single) arrival and once every posted byte has landed.
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar),
+                 "r"(bytes)
+                 : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -368,6 +376,24 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
         if (early_meta)
             for (int b = 0; b < ahead_rows; ++b)
                 fetch_meta(b);
+        // With the caller's promise that the residual was complete before the previous
+        // kernel began, the residual rows of the first (up to ns) rows are copied into
+        // their stages before griddepcontrol.wait; their bytes are posted without an
+        // arrival, which those rows' own arrive.expect_tx (for the other slots) adds.
+        int early_rows = 0;
+        if (!kChunked && p.residual_ready && has_res) {
+            int64_t r = row;
+            for (; early_rows < ns && r < rows; ++early_rows) {
+                if (lane == 0) {
+                    const uint32_t bar = full0 + 8 * early_rows;
+                    mbar_expect_tx(bar, slot_bytes);
+                    bulk_g2s(stage0 + static_cast<uint32_t>(early_rows) * stage_bytes +
+                                 static_cast<uint32_t>(n_main) * slot_bytes,
+                             p.residual_in + r * H, slot_bytes, bar);
+                }
+                r = next_row(p, r + gridDim.x);
+            }
+        }
         pdl_wait();
         if (!early_meta)
             for (int b = 0; b < ahead_rows; ++b)
@@ -419,8 +445,11 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
                 const int64_t c0 = static_cast<int64_t>(c) * chunk;    // first column
                 const uint32_t bytes =
                     static_cast<uint32_t>((H - c0 < chunk ? H - c0 : chunk) * 2);
+                // (a row whose residual went out early posts and copies the rest)
+                const bool res_early = issued < early_rows;
+                const unsigned posted = res_early ? valid & ~(1u << n_main) : valid;
                 if (lane == 0)
-                    mbar_arrive_expect_tx(full, bytes * __popc(valid));
+                    mbar_arrive_expect_tx(full, bytes * __popc(posted));
 #ifdef LB_TEST_HOOKS
                 if (row == p.test_withhold_row)
                     src = nullptr;               // the posted bytes never arrive
@@ -429,14 +458,14 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
                 if (lane_issue) {
                     // short slots: lane j issues slot j's copy, all at once
                     __syncwarp();
-                    if (src != nullptr)
+                    if (src != nullptr && !(res_early && lane == n_main))
                         bulk_g2s(dst + lane * slot_bytes,
                                  reinterpret_cast<const uint16_t *>(src) + c0, bytes, full);
                 } else {
                     for (int j = 0; j < n_slots; ++j) {
                         const uint16_t *sj = reinterpret_cast<const uint16_t *>(__shfl_sync(
                             0xFFFFFFFFu, reinterpret_cast<unsigned long long>(src), j));
-                        if (lane == 0 && sj != nullptr)
+                        if (lane == 0 && sj != nullptr && !(res_early && j == n_main))
                             bulk_g2s(dst + j * slot_bytes, sj + c0, bytes, full);
                     }
                 }

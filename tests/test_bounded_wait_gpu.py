@@ -32,6 +32,7 @@ L = lb.load(build.build(test_hooks=True))
 L.lb_test_withhold_row.argtypes = [ctypes.c_int64]
 L.lb_test_withhold_row.restype = None
 K, T, H, eps, ROW = 2, 300, int(sys.argv[2]), 1e-6, 5
+PROMISE = sys.argv[3] == "1"      # residual promise: the rows' residual copies go out early
 w = wl.fold_workload("timeout", K, T, H, seed=77)
 want = oracle.fold_norm(w.partials, w.residual, w.gamma, eps)
 P = [dev_bits(p) for p in w.partials]
@@ -42,7 +43,7 @@ plan = lb.lb_launch_plan(T, H, K + 1, torch.cuda.get_device_properties(0).multi_
 
 def call():
     ro, yo = Guarded(T, H, torch.bfloat16), Guarded(T, H, torch.bfloat16)
-    lb.lb_fold_norm(P, R, ro.t, G, yo.t, T, H, eps)
+    lb.lb_fold_norm(P, R, ro.t, G, yo.t, T, H, eps, residual_ready=PROMISE)
     return ro, yo
 
 def rows_state(ro, yo):
@@ -80,11 +81,14 @@ print(json.dumps({"kernel": plan.kernel, "chunks": plan.chunks, "err": err, "ela
 """
 
 
-@pytest.mark.parametrize("H,chunks", [(2048, 1), (4096, 1), (12288, 3)])
-# whole rows with a copy per producer lane, whole rows with lane 0 issuing, chunked rows
-def test_a_withheld_row_times_out_and_the_context_survives(H, chunks):
-    r = subprocess.run([sys.executable, "-c", _SCRIPT, ROOT, str(H)], capture_output=True,
-                       text=True, timeout=600)
+@pytest.mark.parametrize("H,chunks,promise", [(2048, 1, False), (4096, 1, False),
+                                              (12288, 3, False), (4096, 1, True)])
+# whole rows with a copy per producer lane, whole rows with lane 0 issuing, chunked rows,
+# and whole rows whose residual copies went out before the rest (the withheld row's
+# residual lands, its stage must still wait for the bytes that never come)
+def test_a_withheld_row_times_out_and_the_context_survives(H, chunks, promise):
+    r = subprocess.run([sys.executable, "-c", _SCRIPT, ROOT, str(H), "1" if promise else "0"],
+                       capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-4000:]
     got = json.loads(r.stdout.strip().splitlines()[-1])
     from layer_boundary_fusion_gb300 import lb

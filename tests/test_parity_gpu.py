@@ -175,7 +175,7 @@ def test_ragged_slice_every_rank(lb, fp8):
 
 
 def _gpu_moe(lb, w, *, idx=None, residual=True, fp8=False, flag=False, want_y=True,
-             routing_ready=False):
+             routing_ready=False, residual_ready=False):
     T, H = w.T, w.H
     idx = w.idx if idx is None else idx
     E = dev_bits(w.expert_out)
@@ -192,7 +192,7 @@ def _gpu_moe(lb, w, *, idx=None, residual=True, fp8=False, flag=False, want_y=Tr
     lb.lb_moe_finalize_fold_norm(E, w.expert_out.shape[0], I, Wt, idx.shape[1], R, ro.t, G,
                                  yo.t if yo else None, qo.t if fp8 else None,
                                  so.t if fp8 else None, T, H, w.eps, F,
-                                 routing_ready=routing_ready)
+                                 routing_ready=routing_ready, residual_ready=residual_ready)
     torch.cuda.synchronize()
     _assert_unchanged(before, [E, I, Wt, R, G])
     out = {"residual_out": ro}
@@ -333,6 +333,40 @@ def test_residual_ready(lb, T, H, fp8):
     plain = _options_fold(lb, w, fp8=fp8, gemma=True, snapshot=False)
     for k in got:
         assert_bits_equal(got[k], plain[k], f"residual ready vs default: {k}")
+
+
+def test_promises_on_slices_and_moe(lb):
+    """The residual (and, for MoE, routing) promise on the slice and MoE calls of the
+    stream kernel, whose first rows' residual copies then go out early: results equal
+    the oracle and the default call bit for bit."""
+    w = wl.ragged_slice(seed=13, slice_=3)
+    P = [dev_bits(p) for p in w.partials]
+    R = dev_bits(w.residual)
+    G = torch.from_numpy(w.gamma).cuda()
+    outs = []
+    for ready in (False, True):
+        ro, yo = Guarded(w.T, w.H, torch.bfloat16), Guarded(w.T, w.H, torch.bfloat16)
+        lb.lb_slice_fold_norm(P, w.T_pad, w.num_slices, w.slice, w.set_offsets, w.set_counts,
+                              R, ro.t, G, yo.t, None, None, w.H, w.eps, residual_ready=ready)
+        torch.cuda.synchronize()
+        ro.check(), yo.check()
+        outs.append((ro.host(), yo.host()))
+    assert plan(lb, w.T, w.H, w.K + 1).kernel == lb.LB_KERNEL_STREAM
+    want = oracle.slice_fold_norm(w.partials, w.T_pad, w.num_slices, w.slice, w.set_offsets,
+                                  w.set_counts, w.residual, w.gamma, w.eps)
+    assert_bits_equal(outs[1][0], want["residual_out"], "slice, promised: residual'")
+    assert_bf16_close(outs[1][1], want["y"], "slice, promised: y")
+    assert_bits_equal(outs[1][0], outs[0][0], "slice: promised vs default residual'")
+    assert_bits_equal(outs[1][1], outs[0][1], "slice: promised vs default y")
+    m = wl.moe_workload("promise_moe", 600, 4096, 64, 8, seed=46)
+    want = oracle.moe_finalize_fold_norm(m.expert_out, m.idx, m.w, m.residual, m.gamma, m.eps,
+                                         want_fp8=True)
+    for fp8 in (False, True):
+        got = _gpu_moe(lb, m, fp8=fp8, routing_ready=True, residual_ready=True)
+        check_fold(got, want, f"moe, both promises, fp8={fp8}")
+        plain = _gpu_moe(lb, m, fp8=fp8)
+        for k in got:
+            assert_bits_equal(got[k], plain[k], f"moe promised vs default: {k}")
 
 
 def test_moe_bad_index_on_the_stream_kernel(lb):
