@@ -5,17 +5,20 @@
 //   warp 0 (producer): for each of this CTA's rows, wait until its stage is free,
 //     post the byte count on the stage's "full" mbarrier and issue one
 //     cp.async.bulk (global -> shared) per input row: the K partial rows (or the
-//     gathered expert rows of a MoE finalize) and the residual row.  A MoE token's
+//     gathered expert rows of a MoE finalize) and the residual row (lane 0 in turn,
+//     or one lane per row for short slots and for expert rows).  A MoE token's
 //     expert indices and routing weights are fetched two rows ahead (cp.async) into
-//     a ring of per-row metadata blocks beside the stages.
+//     a ring of per-row metadata blocks beside the stages.  On the caller's promises
+//     the first rows' routing and residual rows go out before griddepcontrol.wait.
 //   consumer groups of W warps (rows dealt to the groups in turn, so that several
 //     rows are reduced at once): wait on "full", fold the stage's rows in binary32 in
 //     the definition's order, hand the stage back ("empty" mbarrier, one arrive per
 //     warp), store residual', reduce sum(o^2) (and max|o*gamma| for FP8) across the
 //     group with shuffles and ONE named barrier per row, and store the bf16 read or
-//     the FP8 codes and scale.  gamma stays in registers for the whole kernel.
+//     the FP8 codes and scale.  gamma stays in registers for the whole kernel (in
+//     shared memory for rows split into column chunks, one chunk per stage).
 //
-// Loads in flight per SM are bounded by the stages (up to ~200 KB), not by
+// Loads in flight per SM are bounded by the stages (up to ~220 KB), not by
 // registers, and the fixed per-row costs (one barrier, one rsqrt) are spread over
 // 8-32 elements per consumer thread.
 //
