@@ -6,6 +6,17 @@ address or ``None`` for NULL are accepted wherever the C side takes a pointer),
 passes the stream, and raises :class:`LBError` on a non-OK status.  All work runs in
 the library's kernels; there is no fallback.  If the library has not been built the
 first call raises :class:`LibraryMissing`.
+
+The ``lb_options`` argument of the calls is built from keywords:
+
+* ``gemma=True`` -- LB_OPT_GEMMA_WEIGHT, the read's weight is 1 + gamma;
+* ``residual_snapshot=t`` -- a second bf16 copy of residual' into ``t``;
+* ``residual_ready=True`` -- LB_OPT_RESIDUAL_READY, the caller's promise that the
+  residual and gamma were complete before the kernel preceding the call began;
+* ``routing_ready=True`` (MoE finalize only) -- LB_OPT_ROUTING_READY, the same promise
+  for the routing indices and weights.
+
+Without keywords NULL is passed (the defaults).
 """
 from __future__ import annotations
 
