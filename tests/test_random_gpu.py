@@ -2,12 +2,14 @@
 
 Each case draws a shape (K, T, H with H % 8 == 0), a stream mode (Initial or not,
 bf16 read, FP8 read, both, none) and the options (Gemma weight, residual snapshot,
-in-place residual) from a fixed seed, runs the call through the C ABI with guard rows
+in-place residual, the residual and routing promises) from a fixed seed, runs the call through the C ABI with guard rows
 around every output, and compares element by element with the oracle under the parity
 bar of tests/parity_util.py.  The shapes straddle both kernels (rows below and above
 the SM count), 1, 2 and 4 vectors per thread and ragged last vectors of a warp.  MoE
 and ragged-slice cases draw their routing and set layouts the same way.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -20,6 +22,8 @@ from parity_util import (Guarded, assert_bf16_close, assert_bits_equal, assert_f
 pytestmark = pytest.mark.gpu
 
 MAX_ELEMS = 3_000_000      # rows x H per case: the oracle finishes each in about a second
+# cases per sweep (a deeper one-off run: LB_RANDOM_SCALE=10)
+SCALE = int(os.environ.get("LB_RANDOM_SCALE", "1"))
 
 
 @pytest.fixture(scope="module")
@@ -56,7 +60,7 @@ def _compare(got, want, what, res_exact=True):
         assert_fp8_close(got["q"], want["q"], got["scale"], want["scale"], f"{what} fp8")
 
 
-@pytest.mark.parametrize("case", range(40))
+@pytest.mark.parametrize("case", range(40 * SCALE))
 def test_random_fold(lb, case):
     rng = np.random.default_rng(1000 + case)
     T, H = _draw_shape(rng)
@@ -70,6 +74,7 @@ def test_random_fold(lb, case):
         read = "bf16"
     w = wl.fold_workload("rand", K, T, H, seed=2000 + case, residual=residual,
                          outlier_frac=0.02 if rng.random() < 0.3 else 0.0)
+    residual_ready = bool(rng.random() < 0.4)     # the promise changes no result
     fp8 = read in ("fp8", "both")
     want_y = read in ("bf16", "both")
     want = oracle.fold_norm(w.partials, w.residual, w.gamma, w.eps, want_y=True,
@@ -83,7 +88,8 @@ def test_random_fold(lb, case):
     so = Guarded(T, 0, torch.float32) if fp8 else None
     sn = Guarded(T, H, torch.bfloat16) if snapshot else None
     res_out = R if in_place else ro.t
-    kw = dict(gemma=gemma, residual_snapshot=sn.t if sn else None)
+    kw = dict(gemma=gemma, residual_snapshot=sn.t if sn else None,
+              residual_ready=residual_ready)
     if fp8:
         lb.lb_fold_norm_fp8(P, R, res_out, G, qo.t, so.t, yo.t if yo else None, T, H, w.eps,
                             **kw)
@@ -100,10 +106,11 @@ def test_random_fold(lb, case):
     if in_place:
         got["residual_out"] = host_bits(R)
     _compare(got, want, f"case {case}: K={K} T={T} H={H} read={read} res={residual} "
-                        f"gemma={gemma} snap={snapshot} inplace={in_place}")
+                        f"gemma={gemma} snap={snapshot} inplace={in_place} "
+                        f"promise={residual_ready}")
 
 
-@pytest.mark.parametrize("case", range(16))
+@pytest.mark.parametrize("case", range(16 * SCALE))
 def test_random_moe(lb, case):
     rng = np.random.default_rng(3000 + case)
     T, H = _draw_shape(rng)
@@ -115,6 +122,7 @@ def test_random_moe(lb, case):
     fp8 = bool(rng.random() < 0.4)
     gemma = bool(rng.random() < 0.3)
     w = wl.moe_workload("rand_moe", T, H, E, topk, seed=4000 + case, residual=residual)
+    routing_ready, residual_ready = bool(rng.random() < 0.4), bool(rng.random() < 0.4)
     want = oracle.moe_finalize_fold_norm(w.expert_out, w.idx, w.w, w.residual, w.gamma,
                                          w.eps, want_fp8=fp8, gemma=gemma)
     Ex = dev_bits(w.expert_out)
@@ -127,7 +135,8 @@ def test_random_moe(lb, case):
     so = Guarded(T, 0, torch.float32) if fp8 else None
     lb.lb_moe_finalize_fold_norm(Ex, w.expert_out.shape[0], I, Wt, topk, R, ro.t, G, yo.t,
                                  qo.t if fp8 else None, so.t if fp8 else None, T, H, w.eps,
-                                 None, gemma=gemma)
+                                 None, gemma=gemma, routing_ready=routing_ready,
+                                 residual_ready=residual_ready)
     torch.cuda.synchronize()
     got = {}
     for name, g in (("residual_out", ro), ("y", yo), ("q", qo), ("scale", so)):
@@ -135,10 +144,10 @@ def test_random_moe(lb, case):
             g.check()
             got[name] = g.host()
     _compare(got, want, f"moe case {case}: T={T} H={H} E={E} topk={topk} res={residual} "
-                        f"fp8={fp8} gemma={gemma}")
+                        f"fp8={fp8} gemma={gemma} promises={routing_ready},{residual_ready}")
 
 
-@pytest.mark.parametrize("case", range(12))
+@pytest.mark.parametrize("case", range(12 * SCALE))
 def test_random_slices(lb, case):
     rng = np.random.default_rng(5000 + case)
     H = int(rng.choice([64, 1024, 4096]))
@@ -163,7 +172,8 @@ def test_random_slices(lb, case):
         qo = Guarded(S, H, torch.uint8) if fp8 else None
         so = Guarded(S, 0, torch.float32) if fp8 else None
         lb.lb_slice_fold_norm(P, T_pad, num_slices, r, w.set_offsets, w.set_counts, R, ro.t,
-                              G, yo.t, qo.t if fp8 else None, so.t if fp8 else None, H, w.eps)
+                              G, yo.t, qo.t if fp8 else None, so.t if fp8 else None, H, w.eps,
+                              residual_ready=bool(r % 2))
         torch.cuda.synchronize()
         want = oracle.slice_fold_norm(w.partials, T_pad, num_slices, r, w.set_offsets,
                                       w.set_counts, w.residual_full[r * S:(r + 1) * S],
