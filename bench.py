@@ -445,6 +445,14 @@ def measure_variants(lb, dev, stream, dist, steps):
     el, _ = time_graph(ls, steps, 20, stream, dist)
     record("moe_finalize_routing_ready", w.T, nb, el, steps,
            plan_of(lb, w.T, w.H, w.topk + 1, props), f"rotated {ns} sets")
+    ls = [(lambda s=s: lb.lb_moe_finalize_fold_norm(s[0], w.expert_out.shape[0], I, Wt, w.topk,
+                                                   s[1], s[2], G, s[3], None, None, w.T, w.H,
+                                                   w.eps, None, stream=sp, routing_ready=True,
+                                                   residual_ready=True))
+          for s in sets]
+    el, _ = time_graph(ls, steps, 20, stream, dist)
+    record("moe_finalize_both_promises", w.T, nb, el, steps,
+           plan_of(lb, w.T, w.H, w.topk + 1, props), f"rotated {ns} sets")
     del sets, ls, Q
     # a decode-size finalize (T=64 tokens of the same routing recipe) on the row kernel,
     # without and with the routing promise
