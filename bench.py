@@ -42,6 +42,11 @@ from layer_boundary_fusion_gb300 import workloads as wl  # noqa: E402
 METRIC = "boundary tokens/s and achieved HBM GB/s (% of ~8 TB/s) at T=2048,H=4096"
 HEADLINE = "prefill_fold_norm_fp8"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0    # the ~8 TB/s the metric is stated against
+# GPU clock cycles of the delay kernel queued before each timed region (~0.2 ms)
+DELAY_CYCLES = 400_000
+# variants: timed regions of --variant-steps launches each, the median reported
+VARIANT_REPEATS = 5
 
 
 # --------------------------------------------------------------------------------------
@@ -176,10 +181,16 @@ def n_sets(bytes_per_call, dev):
     return max(2, math.ceil(3 * l2 / bytes_per_call))
 
 
-def time_graph(launches, steps, warmup, stream, dist, sampler=None):
+def time_graph(launches, steps, warmup, stream, dist, repeats=1):
     """Replays `steps` launches (cycling over the callables in `launches`) from CUDA
-    graphs after `warmup` eager launches; returns the elapsed seconds measured with
-    CUDA events on `stream`, and the wall-clock window of the timed region."""
+    graphs after `warmup` eager launches, `repeats` times; returns the elapsed seconds
+    of each timed region (CUDA events on `stream`; a float when repeats == 1) and the
+    wall-clock window of the last one.
+
+    Before each start event the stream gets a self-terminating delay kernel (torch's
+    clock-bounded sleep, ~0.2 ms) that keeps the GPU busy while the host submits the
+    replays, so the timed region holds the launches alone and not the host's graph
+    submission latency."""
     with torch.cuda.stream(stream):
         for i in range(warmup):
             launches[i % len(launches)]()
@@ -198,23 +209,33 @@ def time_graph(launches, steps, warmup, stream, dist, sampler=None):
                     launches[(done + i) % len(launches)]()
             graphs.append((g, n))
         done += n
-    # one untimed replay of each distinct graph
-    for g, _ in {id(g): (g, n) for g, n in graphs}.values():
-        g.replay()
-    torch.cuda.synchronize()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    dist.barrier()
-    torch.cuda.synchronize()
-    t0 = time.time()
-    start.record(stream)
-    with torch.cuda.stream(stream):
-        for g, _ in graphs:
+    # untimed replays of each distinct graph (at least ~2000 launches in all), so that
+    # the timed region starts with clocks, caches and translations settled
+    distinct = list({id(g): (g, n) for g, n in graphs}.values())
+    for _ in range(max(1, -(-2000 // steps))):
+        for g, _ in distinct:
             g.replay()
-    end.record(stream)
     torch.cuda.synchronize()
-    t1 = time.time()
-    dist.barrier()
-    return start.elapsed_time(end) / 1e3, (t0, t1)
+    out = []
+    window = (0.0, 0.0)
+    for _ in range(repeats):
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        dist.barrier()
+        torch.cuda.synchronize()
+        t0 = time.time()
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(DELAY_CYCLES)
+            start.record(stream)
+            for g, _ in graphs:
+                g.replay()
+            end.record(stream)
+        torch.cuda.synchronize()
+        t1 = time.time()
+        dist.barrier()
+        out.append(start.elapsed_time(end) / 1e3)
+        window = (t0, t1)
+    return (out[0] if repeats == 1 else out), window
 
 
 def plan_of(lb, rows, H, n_inputs, props):
@@ -316,7 +337,13 @@ def measure_variants(lb, dev, stream, dist, steps):
         out[name] = {"rows": rows, "us_per_call": round(t * 1e6, 3),
                      "tokens_per_s": round(rows / t, 1), "gbs": round(nbytes / t / 1e9, 1),
                      "frac_of_measured_hbm": round(nbytes / t / 1e9 / peak, 4),
+                     "frac_of_nominal_hbm": round(nbytes / t / 1e9 / NOMINAL_HBM_GBS, 4),
                      "bytes_per_call": nbytes, "launch": shape, "l2": l2}
+
+    def tg(ls):
+        """Median over VARIANT_REPEATS timed regions of `steps` launches each."""
+        runs, _ = time_graph(ls, steps, 20, stream, dist, repeats=VARIANT_REPEATS)
+        return statistics.median(runs)
 
     props = torch.cuda.get_device_properties(dev)
     # decode: K=8 T=64, with and without a residual; rotated and hot-L2
@@ -326,10 +353,10 @@ def measure_variants(lb, dev, stream, dist, steps):
         ns = n_sets(nb, dev)
         sets = fold_sets(w, dev, ns, False)
         ls = [fold_launcher(lb, s, w.T, w.H, w.eps, False, stream) for s in sets]
-        el, _ = time_graph(ls, steps, 20, stream, dist)
+        el = tg(ls)
         record(name, w.T, nb, el, steps, plan_of(lb, w.T, w.H, w.K + (w.residual is not None), props),
                f"rotated {ns} sets")
-        el, _ = time_graph(ls[:1], steps, 20, stream, dist)
+        el = tg(ls[:1])
         record(name + "_hot_l2", w.T, nb, el, steps,
                plan_of(lb, w.T, w.H, w.K + (w.residual is not None), props),
                "hot: one buffer set, L2-resident")
@@ -339,7 +366,7 @@ def measure_variants(lb, dev, stream, dist, steps):
         ls = [(lambda s=s: lb.lb_fold_norm(s.P, s.R, s.ro, s.G, s.yo, w.T, w.H, w.eps,
                                            stream=stream.cuda_stream, residual_ready=True))
               for s in sets]
-        el, _ = time_graph(ls, steps, 20, stream, dist)
+        el = tg(ls)
         record(name + "_residual_ready", w.T, nb, el, steps,
                plan_of(lb, w.T, w.H, w.K + (w.residual is not None), props),
                f"rotated {ns} sets")
@@ -362,7 +389,7 @@ def measure_variants(lb, dev, stream, dist, steps):
     ls = [(lambda s=s: lb.lb_slice_fold_norm(s[0], w.T_pad, w.num_slices, w.slice,
                                             w.set_offsets, w.set_counts, s[1], s[2], G, s[3],
                                             None, None, w.H, w.eps, stream=sp)) for s in sets]
-    el, _ = time_graph(ls, steps, 20, stream, dist)
+    el = tg(ls)
     record("ragged_slice", v, nb, el, steps, plan_of(lb, S, w.H, w.K + 1, props),
            f"rotated {ns} sets")
     # with the residual promise: the first rows' residual copies go out early
@@ -370,7 +397,7 @@ def measure_variants(lb, dev, stream, dist, steps):
                                             w.set_offsets, w.set_counts, s[1], s[2], G, s[3],
                                             None, None, w.H, w.eps, stream=sp,
                                             residual_ready=True)) for s in sets]
-    el, _ = time_graph(ls, steps, 20, stream, dist)
+    el = tg(ls)
     record("ragged_slice_residual_ready", v, nb, el, steps,
            plan_of(lb, S, w.H, w.K + 1, props), f"rotated {ns} sets")
     # the same slice with the FP8 read
@@ -381,7 +408,7 @@ def measure_variants(lb, dev, stream, dist, steps):
                                                  w.set_offsets, w.set_counts, s[1], s[2], G,
                                                  None, q[0], q[1], w.H, w.eps, stream=sp))
           for s, q in zip(sets, Q)]
-    el, _ = time_graph(ls, steps, 20, stream, dist)
+    el = tg(ls)
     record("ragged_slice_fp8", v, nb8, el, steps, plan_of(lb, S, w.H, w.K + 1, props),
            f"rotated {ns} sets")
     del sets, ls, P0, Q
@@ -397,7 +424,7 @@ def measure_variants(lb, dev, stream, dist, steps):
         ls = [(lambda s=s, rank=rank: lb.lb_slice_fold_norm_v(
             s[0], w.T_pad, rank, w.set_offsets, w.set_counts, s[1], s[2], G, s[3], None, None,
             w.H, w.eps, stream=sp)) for s in sets]
-        el, _ = time_graph(ls, steps, 20, stream, dist)
+        el = tg(ls)
         record(f"ragged_rsv_rank{rank}", c, nb, el, steps, plan_of(lb, c, w.H, w.K + 1, props),
                f"rotated {ns} sets")
         del sets, ls, P0
@@ -414,7 +441,7 @@ def measure_variants(lb, dev, stream, dist, steps):
     ls = [(lambda s=s: lb.lb_moe_finalize_fold_norm(s[0], w.expert_out.shape[0], I, Wt, w.topk,
                                                    s[1], s[2], G, s[3], None, None, w.T, w.H,
                                                    w.eps, None, stream=sp)) for s in sets]
-    el, _ = time_graph(ls, steps, 20, stream, dist)
+    el = tg(ls)
     record("moe_finalize", w.T, nb, el, steps, plan_of(lb, w.T, w.H, w.topk + 1, props),
            f"rotated {ns} sets")
     # the terminal handoff: the same finalize feeding a Gemma final norm (1 + gamma)
@@ -422,7 +449,7 @@ def measure_variants(lb, dev, stream, dist, steps):
                                                    s[1], s[2], G, s[3], None, None, w.T, w.H,
                                                    w.eps, None, stream=sp, gemma=True))
           for s in sets]
-    el, _ = time_graph(ls, steps, 20, stream, dist)
+    el = tg(ls)
     record("moe_finalize_gemma", w.T, nb, el, steps, plan_of(lb, w.T, w.H, w.topk + 1, props),
            f"rotated {ns} sets")
     # the FP8 read on the finalize (codes + scales instead of the bf16 read)
@@ -432,7 +459,7 @@ def measure_variants(lb, dev, stream, dist, steps):
     ls = [(lambda s=s, q=q: lb.lb_moe_finalize_fold_norm(
         s[0], w.expert_out.shape[0], I, Wt, w.topk, s[1], s[2], G, None, q[0], q[1], w.T, w.H,
         w.eps, None, stream=sp)) for s, q in zip(sets, Q)]
-    el, _ = time_graph(ls, steps, 20, stream, dist)
+    el = tg(ls)
     record("moe_finalize_fp8", w.T, nb8, el, steps, plan_of(lb, w.T, w.H, w.topk + 1, props),
            f"rotated {ns} sets")
     # with the routing promise (LB_OPT_ROUTING_READY: idx and w are never written by the
@@ -442,7 +469,7 @@ def measure_variants(lb, dev, stream, dist, steps):
                                                    s[1], s[2], G, s[3], None, None, w.T, w.H,
                                                    w.eps, None, stream=sp, routing_ready=True))
           for s in sets]
-    el, _ = time_graph(ls, steps, 20, stream, dist)
+    el = tg(ls)
     record("moe_finalize_routing_ready", w.T, nb, el, steps,
            plan_of(lb, w.T, w.H, w.topk + 1, props), f"rotated {ns} sets")
     ls = [(lambda s=s: lb.lb_moe_finalize_fold_norm(s[0], w.expert_out.shape[0], I, Wt, w.topk,
@@ -450,7 +477,7 @@ def measure_variants(lb, dev, stream, dist, steps):
                                                    w.eps, None, stream=sp, routing_ready=True,
                                                    residual_ready=True))
           for s in sets]
-    el, _ = time_graph(ls, steps, 20, stream, dist)
+    el = tg(ls)
     record("moe_finalize_both_promises", w.T, nb, el, steps,
            plan_of(lb, w.T, w.H, w.topk + 1, props), f"rotated {ns} sets")
     del sets, ls, Q
@@ -472,7 +499,7 @@ def measure_variants(lb, dev, stream, dist, steps):
             s[0], T64 * w.topk, I64, W64, w.topk, s[1], s[2], G, s[3], None, None,
             T64, w.H, w.eps, None, stream=sp, routing_ready=ready,
             residual_ready=res_ready)) for s in sets]
-        el, _ = time_graph(ls, steps, 20, stream, dist)
+        el = tg(ls)
         record(name, T64, nb64, el, steps, plan_of(lb, T64, w.H, w.topk + 1, props),
                f"rotated {ns64} sets")
     del sets, ls
@@ -486,7 +513,7 @@ def measure_variants(lb, dev, stream, dist, steps):
     ls = [(lambda s=s: lb.lb_fold_norm_fp8(s.P, s.R, s.ro, s.G, s.qo, s.so, None, w.T, w.H,
                                           w.eps, stream=sp, gemma=True,
                                           residual_snapshot=s.snap)) for s in sets]
-    el, _ = time_graph(ls, steps, 20, stream, dist)
+    el = tg(ls)
     record("prefill_fp8_gemma_snapshot", w.T, nb, el, steps,
            plan_of(lb, w.T, w.H, w.K + 1, props), f"rotated {ns} sets")
     # the headline call with the residual promise
@@ -494,7 +521,7 @@ def measure_variants(lb, dev, stream, dist, steps):
     ls = [(lambda s=s: lb.lb_fold_norm_fp8(s.P, s.R, s.ro, s.G, s.qo, s.so, None, w.T, w.H,
                                           w.eps, stream=sp, residual_ready=True))
           for s in sets]
-    el, _ = time_graph(ls, steps, 20, stream, dist)
+    el = tg(ls)
     record("prefill_fp8_residual_ready", w.T, nb, el, steps,
            plan_of(lb, w.T, w.H, w.K + 1, props), f"rotated {ns} sets")
     del sets, ls
@@ -508,7 +535,7 @@ def measure_variants(lb, dev, stream, dist, steps):
         ns = n_sets(moved, dev)
         sets = fold_sets(w, dev, ns, False)
         fused = [fold_launcher(lb, s, w.T, w.H, w.eps, False, stream) for s in sets]
-        el, _ = time_graph(fused, steps, 20, stream, dist)
+        el = tg(fused)
         record(f"{name}_fused", w.T, nb, el, steps,
                plan_of(lb, w.T, w.H, w.K + 1, props), f"rotated {ns} sets")
         for s in sets:
@@ -518,7 +545,7 @@ def measure_variants(lb, dev, stream, dist, steps):
             lb.lb_fold_norm(s.P, None, s.sum, None, None, w.T, w.H, w.eps, stream=sp)
             lb.lb_fold_norm([s.sum], s.R, s.ro, s.G, s.yo, w.T, w.H, w.eps, stream=sp)
         ls = [(lambda s=s: unfused(s)) for s in sets]
-        el, _ = time_graph(ls, steps, 20, stream, dist)
+        el = tg(ls)
         record(f"{name}_unfused", w.T, nb, el, steps,
                [plan_of(lb, w.T, w.H, w.K, props), plan_of(lb, w.T, w.H, 2, props)],
                f"rotated {ns} sets")
@@ -531,10 +558,39 @@ def measure_variants(lb, dev, stream, dist, steps):
     nb = bytes_fold(w.K, w.T, w.H)
     sets = fold_sets(w, dev, 1, False)
     ls = [fold_launcher(lb, sets[0], w.T, w.H, w.eps, False, stream)]
-    el, _ = time_graph(ls, steps, 20, stream, dist)
+    el = tg(ls)
     record("tiny_fold_norm", w.T, nb, el, steps, plan_of(lb, w.T, w.H, w.K + 1, props),
            "hot: one buffer set, L2-resident")
     torch.cuda.empty_cache()
+    return out
+
+
+# The five specified workloads and the bench entries that time them.
+CONFIGS = (
+    ("cfg1_tiny_K2_T16_H512", "tiny_fold_norm"),
+    ("cfg2_decode_K8_T64", "decode_fold_norm"),
+    ("cfg2_decode_initial_K8_T64", "decode_initial"),
+    ("cfg3_prefill_fp8_K4_T2048", None),               # the headline call itself
+    ("cfg4_ragged_slice_r3_K8_S254", "ragged_slice"),
+    ("cfg5_moe_finalize_T1024_top8", "moe_finalize"),
+)
+
+
+def config_summary(variants, headline):
+    """One compact entry per specified workload: us per call, GB/s, fractions of the
+    measured copy peak and of the nominal 8 TB/s, the kernel and the L2 mode."""
+    out = {}
+    for name, key in CONFIGS:
+        v = headline if key is None else variants.get(key)
+        if v is None:
+            continue
+        launch = v["launch"]
+        kind = "stream" if launch.get("kernel") == 1 else "row"
+        out[name] = {"us": v["us_per_call"], "gbs": v["gbs"],
+                     "frac_measured": v["frac_of_measured_hbm"],
+                     "frac_8tbs": v["frac_of_nominal_hbm"],
+                     "kernel": f"{kind} grid {launch.get('grid')}",
+                     "l2": "hot" if v["l2"].startswith("hot") else "rotated"}
     return out
 
 
@@ -687,10 +743,14 @@ def run_native(args, dist):
                          f"{props.L2_cache_size / 1e6:.0f} MB)",
                    "launch": plan_of(lb, w.T, w.H, w.K + 1, props),
                    "timing": "CUDA graphs of up to 500 launches, CUDA events on the "
-                             "launching stream",
+                             "launching stream, a clock-bounded delay kernel queued before "
+                             "the start event; variants: median of "
+                             f"{VARIANT_REPEATS} timed regions",
                    "parallelism": f"replica per GPU x{dist.world} (rows independent)"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
+                     "nominal_peak": NOMINAL_HBM_GBS,
                      "traffic": ncu_traffic(HEADLINE), "peak_source": peak_src,
                      "algorithmic_bytes_per_launch": nbytes,
                      "kernel": kernel_name(plan_of(lb, w.T, w.H, w.K + 1, props), "fold", True)},
@@ -707,6 +767,13 @@ def run_native(args, dist):
         "cpu_baseline": cpu,
         "variants": variants,
     }
+    headline = {"us_per_call": round(per_launch * 1e6, 3), "gbs": round(achieved, 1),
+                "frac_of_measured_hbm": round(achieved / peak, 4),
+                "frac_of_nominal_hbm": round(achieved / NOMINAL_HBM_GBS, 4),
+                "launch": plan_of(lb, w.T, w.H, w.K + 1, props),
+                "l2": f"rotated {ns} sets"}
+    # last key of the line: the five specified workloads at a glance
+    line["configs"] = config_summary(variants, headline)
     if dist.rank == 0:
         print(json.dumps(line), flush=True)
     dist.close()

@@ -16,7 +16,11 @@
  *  - Ownership: the caller allocates and owns every buffer.  The library allocates
  *    nothing, keeps no per-call state and never synchronises the stream.
  *  - Execution: kernels are enqueued asynchronously on `stream` (NULL = the legacy
- *    default stream).  A returned LB_OK means the launch was enqueued.
+ *    default stream), on the device that owns the stream; every buffer must live on
+ *    (or be accessible from) that device.  If the stream's device is not the calling
+ *    thread's current device, the call makes it current for the launch and restores
+ *    the caller's device before returning.  A returned LB_OK means the launch was
+ *    enqueued.
  *  - Arithmetic ("Residual update and input read": the fused add+norm keeps its FP32
  *    accumulation and normalises it, not a rounded snapshot):
  *      o[t,h]  = (+0 + p_0[t,h] + p_1[t,h] + ... + p_{K-1}[t,h]) + res[t,h]
@@ -107,6 +111,12 @@ int lb_version(void);
  * began, as they are between two layer boundaries (GEMMs run in between; gamma is a
  * weight).  The call may then read them without waiting for that kernel to finish.
  * The partials (or expert rows) and every output still wait for it.
+ * Every kernel of this library lets its own dependent start as soon as it begins
+ * (programmatic dependent launch), so a preceding call of this library counts as having
+ * begun while its own predecessor was still running.  Do not set the flag when
+ * residual_in (or gamma) was written by a call of this library earlier in the same
+ * chain of back-to-back launches, unless another kernel runs in between (the usual
+ * case: the layer's GEMMs separate two boundaries).
  */
 #define LB_OPT_RESIDUAL_READY 4u
 

@@ -88,20 +88,16 @@ struct DeviceInfo {
     int device;
 };
 
-int device_info(DeviceInfo *out) {
+int device_info(int dev, DeviceInfo *out) {
     static std::atomic<int> cached[64];
     static DeviceInfo info[64];
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess)
-        return static_cast<int>(e);
     if (dev >= 0 && dev < 64 && cached[dev].load(std::memory_order_acquire)) {
         *out = info[dev];
         return 0;
     }
     DeviceInfo d{};
     d.device = dev;
-    e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaError_t e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess)
         e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess)
@@ -114,6 +110,29 @@ int device_info(DeviceInfo *out) {
     return 0;
 }
 
+// The launch goes to the device that owns `stream` (the current device for the legacy
+// and per-thread default streams); while it is made, that device is current, and the
+// caller's current device is restored afterwards.
+struct StreamDevice {
+    int stream_dev = 0;
+    int prev_dev = 0;
+    bool switched = false;
+    int open(cudaStream_t stream) {
+        cudaError_t e = cudaGetDevice(&prev_dev);
+        if (e == cudaSuccess)
+            e = cudaStreamGetDevice(stream, &stream_dev);
+        if (e == cudaSuccess && stream_dev != prev_dev) {
+            e = cudaSetDevice(stream_dev);
+            switched = e == cudaSuccess;
+        }
+        return static_cast<int>(e);
+    }
+    ~StreamDevice() {
+        if (switched)
+            cudaSetDevice(prev_dev);
+    }
+};
+
 #ifdef LB_TEST_HOOKS
 // Test builds only: the row whose copies the next stream-kernel launches withhold.
 static int64_t g_test_withhold_row = -1;
@@ -121,8 +140,11 @@ static int64_t g_test_withhold_row = -1;
 
 lb_status launch(const lb::Params &p, lb::Mode mode, bool fp8, int n_inputs,
                  cudaStream_t stream) {
+    StreamDevice sd;
+    int e0 = sd.open(stream);
     DeviceInfo d;
-    const int e0 = device_info(&d);
+    if (e0 == 0)
+        e0 = device_info(sd.stream_dev, &d);
     if (e0 != 0) {
         g_last_cuda_error = e0;
         return LB_ERR_CUDA;

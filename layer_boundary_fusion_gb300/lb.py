@@ -3,7 +3,11 @@
 Argument marshalling only: every function has the name and argument order of the C
 entry point, turns tensors into device pointers (a ``torch.Tensor``, an integer
 address or ``None`` for NULL are accepted wherever the C side takes a pointer),
-passes the stream, and raises :class:`LBError` on a non-OK status.  All work runs in
+passes the stream, and raises :class:`LBError` on a non-OK status.  A tensor argument
+must be a contiguous CUDA tensor of the element type the C side reads (bf16 data as
+``bfloat16`` or its raw ``int16``/``uint16`` bits; gamma, weights and scales
+``float32``; indices and the bad-index flag ``int32``; FP8 codes ``uint8``), and all
+tensors of one call must be on one device: anything else raises before the call.  All work runs in
 the library's kernels; there is no fallback.  If the library has not been built the
 first call raises :class:`LibraryMissing`.
 
@@ -173,12 +177,45 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     return lib
 
 
-def _ptr(x) -> Optional[int]:
-    if x is None:
-        return None
-    if isinstance(x, int):
-        return x
-    return x.data_ptr()
+# element types accepted per kind of tensor argument (bf16 data may come as raw bits)
+_DTYPES = {"bf16": ("bfloat16", "int16", "uint16"), "f32": ("float32",), "i32": ("int32",),
+           "u8": ("uint8",)}
+
+
+class _Marshal:
+    """Turns the tensor arguments of one call into device addresses.  A tensor must be
+    a contiguous CUDA tensor of the element type the C side expects, and every tensor
+    of the call must be on the same device; an ``int`` is passed as a raw address and
+    ``None`` as NULL, unchecked."""
+
+    def __init__(self, func: str):
+        self.func = func
+        self.devices = set()
+
+    def __call__(self, x, kind: str, name: str) -> Optional[int]:
+        if x is None:
+            return None
+        if isinstance(x, int):
+            return x
+        if not getattr(x, "is_cuda", False):
+            raise ValueError(f"{self.func}: {name} must be a CUDA tensor")
+        if not x.is_contiguous():
+            raise ValueError(f"{self.func}: {name} must be contiguous")
+        dt = str(x.dtype).replace("torch.", "")
+        if dt not in _DTYPES[kind]:
+            raise TypeError(f"{self.func}: {name} has dtype {dt}, expected "
+                            f"{' or '.join(_DTYPES[kind])}")
+        self.devices.add(x.device)
+        if len(self.devices) > 1:
+            raise ValueError(f"{self.func}: tensor arguments on different devices "
+                             f"{sorted(str(d) for d in self.devices)}")
+        return x.data_ptr()
+
+    def array(self, items: Sequence, kind: str, name: str) -> ctypes.Array:
+        arr = (_vp * max(1, len(items)))()
+        for i, x in enumerate(items):
+            arr[i] = self(x, kind, f"{name}[{i}]")
+        return arr
 
 
 def _stream(stream, *tensors) -> Optional[int]:
@@ -193,21 +230,14 @@ def _stream(stream, *tensors) -> Optional[int]:
     return None
 
 
-def _ptr_array(items: Sequence) -> ctypes.Array:
-    arr = (_vp * max(1, len(items)))()
-    for i, x in enumerate(items):
-        arr[i] = _ptr(x)
-    return arr
-
-
-def _options(gemma: bool, residual_snapshot, routing_ready: bool = False,
+def _options(m: _Marshal, gemma: bool, residual_snapshot, routing_ready: bool = False,
              residual_ready: bool = False):
     """lb_options for the keyword arguments, or None (NULL) for the defaults."""
     if not gemma and residual_snapshot is None and not routing_ready and not residual_ready:
         return None
     flags = ((LB_OPT_GEMMA_WEIGHT if gemma else 0) | (LB_OPT_ROUTING_READY if routing_ready else 0)
              | (LB_OPT_RESIDUAL_READY if residual_ready else 0))
-    return ctypes.byref(Options(flags, _ptr(residual_snapshot)))
+    return ctypes.byref(Options(flags, m(residual_snapshot, "bf16", "residual_snapshot")))
 
 
 def _check(status: int, func: str) -> None:
@@ -244,10 +274,13 @@ def lb_fold_norm(partials, residual_in, residual_out, gamma, y_out, T, H, eps,
                  residual_ready=False) -> None:
     lib = load()
     partials = list(partials)
+    m = _Marshal("lb_fold_norm")
     s = _stream(stream, *partials, residual_in, residual_out, y_out)
-    _check(lib.lb_fold_norm(_ptr_array(partials), len(partials), _ptr(residual_in),
-                            _ptr(residual_out), _ptr(gamma), _ptr(y_out), T, H, eps,
-                            _options(gemma, residual_snapshot, False, residual_ready), s),
+    _check(lib.lb_fold_norm(m.array(partials, "bf16", "partials"), len(partials),
+                            m(residual_in, "bf16", "residual_in"),
+                            m(residual_out, "bf16", "residual_out"), m(gamma, "f32", "gamma"),
+                            m(y_out, "bf16", "y_out"), T, H, eps,
+                            _options(m, gemma, residual_snapshot, False, residual_ready), s),
            "lb_fold_norm")
 
 
@@ -256,11 +289,15 @@ def lb_fold_norm_fp8(partials, residual_in, residual_out, gamma, q_out, scale_ou
                      residual_ready=False) -> None:
     lib = load()
     partials = list(partials)
+    m = _Marshal("lb_fold_norm_fp8")
     s = _stream(stream, *partials, residual_in, residual_out, q_out)
-    _check(lib.lb_fold_norm_fp8(_ptr_array(partials), len(partials), _ptr(residual_in),
-                                _ptr(residual_out), _ptr(gamma), _ptr(q_out),
-                                _ptr(scale_out), _ptr(y_out), T, H, eps,
-                                _options(gemma, residual_snapshot, False, residual_ready), s),
+    _check(lib.lb_fold_norm_fp8(m.array(partials, "bf16", "partials"), len(partials),
+                                m(residual_in, "bf16", "residual_in"),
+                                m(residual_out, "bf16", "residual_out"),
+                                m(gamma, "f32", "gamma"), m(q_out, "u8", "q_out"),
+                                m(scale_out, "f32", "scale_out"), m(y_out, "bf16", "y_out"),
+                                T, H, eps,
+                                _options(m, gemma, residual_snapshot, False, residual_ready), s),
            "lb_fold_norm_fp8")
 
 
@@ -270,13 +307,16 @@ def lb_moe_finalize_fold_norm(expert_out, n_expert_rows, idx, w, topk, residual_
                               residual_snapshot=None, routing_ready=False,
                               residual_ready=False) -> None:
     lib = load()
+    m = _Marshal("lb_moe_finalize_fold_norm")
     s = _stream(stream, expert_out, residual_out, y_out, q_out)
-    _check(lib.lb_moe_finalize_fold_norm(_ptr(expert_out), n_expert_rows, _ptr(idx), _ptr(w),
-                                         topk, _ptr(residual_in), _ptr(residual_out),
-                                         _ptr(gamma), _ptr(y_out), _ptr(q_out),
-                                         _ptr(scale_out), T, H, eps, _ptr(bad_index_flag),
-                                         _options(gemma, residual_snapshot, routing_ready, residual_ready), s),
-           "lb_moe_finalize_fold_norm")
+    _check(lib.lb_moe_finalize_fold_norm(
+        m(expert_out, "bf16", "expert_out"), n_expert_rows, m(idx, "i32", "idx"),
+        m(w, "f32", "w"), topk, m(residual_in, "bf16", "residual_in"),
+        m(residual_out, "bf16", "residual_out"), m(gamma, "f32", "gamma"),
+        m(y_out, "bf16", "y_out"), m(q_out, "u8", "q_out"), m(scale_out, "f32", "scale_out"),
+        T, H, eps, m(bad_index_flag, "i32", "bad_index_flag"),
+        _options(m, gemma, residual_snapshot, routing_ready, residual_ready), s),
+        "lb_moe_finalize_fold_norm")
 
 
 def _int32_array(values):
@@ -294,12 +334,18 @@ def lb_slice_fold_norm(partials, T_pad, num_slices, slice_, set_offsets, set_cou
         raise ValueError("set_offsets and set_counts differ in length")
     offs, n = _int32_array(set_offsets)
     cnts, _ = _int32_array(set_counts)
+    m = _Marshal("lb_slice_fold_norm")
     s = _stream(stream, *partials, residual_out, y_out, q_out)
-    _check(lib.lb_slice_fold_norm(_ptr_array(partials), len(partials), T_pad, num_slices,
-                                  slice_, ctypes.cast(offs, _vp), ctypes.cast(cnts, _vp), n,
-                                  _ptr(residual_in), _ptr(residual_out), _ptr(gamma),
-                                  _ptr(y_out), _ptr(q_out), _ptr(scale_out), H, eps,
-                                  _options(gemma, residual_snapshot, False, residual_ready), s),
+    _check(lib.lb_slice_fold_norm(m.array(partials, "bf16", "partials"), len(partials), T_pad,
+                                  num_slices, slice_, ctypes.cast(offs, _vp),
+                                  ctypes.cast(cnts, _vp), n,
+                                  m(residual_in, "bf16", "residual_in"),
+                                  m(residual_out, "bf16", "residual_out"),
+                                  m(gamma, "f32", "gamma"), m(y_out, "bf16", "y_out"),
+                                  m(q_out, "u8", "q_out"), m(scale_out, "f32", "scale_out"),
+                                  H, eps,
+                                  _options(m, gemma, residual_snapshot, False, residual_ready),
+                                  s),
            "lb_slice_fold_norm")
 
 
@@ -313,12 +359,17 @@ def lb_slice_fold_norm_v(partials, T_pad, set_, set_offsets, set_counts, residua
         raise ValueError("set_offsets and set_counts differ in length")
     offs, n = _int32_array(set_offsets)
     cnts, _ = _int32_array(set_counts)
+    m = _Marshal("lb_slice_fold_norm_v")
     s = _stream(stream, *partials, residual_out, y_out, q_out)
-    _check(lib.lb_slice_fold_norm_v(_ptr_array(partials), len(partials), T_pad, set_,
-                                    ctypes.cast(offs, _vp), ctypes.cast(cnts, _vp), n,
-                                    _ptr(residual_in), _ptr(residual_out), _ptr(gamma),
-                                    _ptr(y_out), _ptr(q_out), _ptr(scale_out), H, eps,
-                                    _options(gemma, residual_snapshot, False, residual_ready), s),
+    _check(lib.lb_slice_fold_norm_v(m.array(partials, "bf16", "partials"), len(partials), T_pad,
+                                    set_, ctypes.cast(offs, _vp), ctypes.cast(cnts, _vp), n,
+                                    m(residual_in, "bf16", "residual_in"),
+                                    m(residual_out, "bf16", "residual_out"),
+                                    m(gamma, "f32", "gamma"), m(y_out, "bf16", "y_out"),
+                                    m(q_out, "u8", "q_out"), m(scale_out, "f32", "scale_out"),
+                                    H, eps,
+                                    _options(m, gemma, residual_snapshot, False,
+                                             residual_ready), s),
            "lb_slice_fold_norm_v")
 
 
@@ -334,7 +385,9 @@ def _handle(func: str, call) -> int:
 
 
 def lb_residual_init(s: ResidualStream, residual, T, H) -> None:
-    _check(load().lb_residual_init(ctypes.byref(s), _ptr(residual), T, H), "lb_residual_init")
+    m = _Marshal("lb_residual_init")
+    _check(load().lb_residual_init(ctypes.byref(s), m(residual, "bf16", "residual"), T, H),
+           "lb_residual_init")
 
 
 def lb_residual_start(s: ResidualStream) -> int:
@@ -343,30 +396,36 @@ def lb_residual_start(s: ResidualStream) -> int:
 
 def lb_residual_leave(s: ResidualStream, h: int, partials) -> int:
     partials = list(partials)
-    arr = _ptr_array(partials)
+    arr = _Marshal("lb_residual_leave").array(partials, "bf16", "partials")
     return _handle("lb_residual_leave", lambda o: load().lb_residual_leave(
         ctypes.byref(s), h, arr, len(partials), o))
 
 
 def lb_residual_leave_moe(s: ResidualStream, h: int, expert_out, n_expert_rows, idx, w,
                           topk) -> int:
+    m = _Marshal("lb_residual_leave_moe")
+    e, i, wt = m(expert_out, "bf16", "expert_out"), m(idx, "i32", "idx"), m(w, "f32", "w")
     return _handle("lb_residual_leave_moe", lambda o: load().lb_residual_leave_moe(
-        ctypes.byref(s), h, _ptr(expert_out), n_expert_rows, _ptr(idx), _ptr(w), topk, o))
+        ctypes.byref(s), h, e, n_expert_rows, i, wt, topk, o))
 
 
 def lb_residual_prepare(s: ResidualStream, h: int, gamma, y_out, q_out, scale_out, eps,
                         stream=None, *, gemma=False, residual_snapshot=None,
                         residual_ready=False) -> int:
     st = _stream(stream, gamma, y_out, q_out)
+    m = _Marshal("lb_residual_prepare")
+    args = (m(gamma, "f32", "gamma"), m(y_out, "bf16", "y_out"), m(q_out, "u8", "q_out"),
+            m(scale_out, "f32", "scale_out"))
+    opt = _options(m, gemma, residual_snapshot, False, residual_ready)
     return _handle("lb_residual_prepare", lambda o: load().lb_residual_prepare(
-        ctypes.byref(s), h, _ptr(gamma), _ptr(y_out), _ptr(q_out), _ptr(scale_out), eps,
-        _options(gemma, residual_snapshot, False, residual_ready), st, o))
+        ctypes.byref(s), h, *args, eps, opt, st, o))
 
 
 def lb_residual_complete_output(s: ResidualStream, h: int, sum_out, stream=None) -> int:
     st = _stream(stream, sum_out)
+    p = _Marshal("lb_residual_complete_output")(sum_out, "bf16", "sum_out")
     return _handle("lb_residual_complete_output", lambda o: load().lb_residual_complete_output(
-        ctypes.byref(s), h, _ptr(sum_out), st, o))
+        ctypes.byref(s), h, p, st, o))
 
 
 def lb_residual_fold(s: ResidualStream, h: int, stream=None) -> int:
@@ -377,13 +436,15 @@ def lb_residual_fold(s: ResidualStream, h: int, stream=None) -> int:
 
 def lb_residual_add_to_output(s: ResidualStream, h: int, extra, stream=None) -> int:
     st = _stream(stream, extra)
+    p = _Marshal("lb_residual_add_to_output")(extra, "bf16", "extra")
     return _handle("lb_residual_add_to_output", lambda o: load().lb_residual_add_to_output(
-        ctypes.byref(s), h, _ptr(extra), st, o))
+        ctypes.byref(s), h, p, st, o))
 
 
 def lb_residual_written(s: ResidualStream, h: int, hidden) -> int:
+    p = _Marshal("lb_residual_written")(hidden, "bf16", "hidden")
     return _handle("lb_residual_written", lambda o: load().lb_residual_written(
-        ctypes.byref(s), h, _ptr(hidden), o))
+        ctypes.byref(s), h, p, o))
 
 
 def lb_residual_take_output(s: ResidualStream, h: int) -> int:
@@ -398,6 +459,9 @@ def lb_residual_norm(s: ResidualStream, h: int, gamma, y_out, q_out, scale_out, 
                      stream=None, *, gemma=False, residual_snapshot=None,
                      residual_ready=False) -> None:
     st = _stream(stream, gamma, y_out, q_out)
-    _check(load().lb_residual_norm(ctypes.byref(s), h, _ptr(gamma), _ptr(y_out), _ptr(q_out),
-                                   _ptr(scale_out), eps, _options(gemma, residual_snapshot, False, residual_ready),
+    m = _Marshal("lb_residual_norm")
+    _check(load().lb_residual_norm(ctypes.byref(s), h, m(gamma, "f32", "gamma"),
+                                   m(y_out, "bf16", "y_out"), m(q_out, "u8", "q_out"),
+                                   m(scale_out, "f32", "scale_out"), eps,
+                                   _options(m, gemma, residual_snapshot, False, residual_ready),
                                    st), "lb_residual_norm")

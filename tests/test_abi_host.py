@@ -283,3 +283,36 @@ def test_binding_fails_loudly_without_the_library(tmp_path):
     r = subprocess.run([sys.executable, "-c", code, ROOT, str(tmp_path / "none.so")],
                        capture_output=True, text=True, timeout=120)
     assert r.stdout.strip() == "missing"
+
+
+class _FakeTensor:
+    """Stands in for a torch tensor in the binding's argument checks (no GPU needed)."""
+
+    def __init__(self, dtype="bfloat16", cuda=True, contiguous=True, device="cuda:0"):
+        self.dtype = f"torch.{dtype}"
+        self.is_cuda = cuda
+        self._contiguous = contiguous
+        self.device = device
+
+    def is_contiguous(self):
+        return self._contiguous
+
+    def data_ptr(self):
+        return 0x10000
+
+
+def test_binding_rejects_bad_tensor_arguments(lib):
+    m = lib._Marshal("lb_fold_norm")
+    assert m(None, "bf16", "y_out") is None
+    assert m(0x1234, "bf16", "y_out") == 0x1234            # raw addresses pass unchecked
+    assert m(_FakeTensor("int16"), "bf16", "residual_in") == 0x10000
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        m(_FakeTensor(cuda=False), "bf16", "residual_in")
+    with pytest.raises(ValueError, match="contiguous"):
+        m(_FakeTensor(contiguous=False), "bf16", "residual_in")
+    with pytest.raises(TypeError, match="float32"):
+        m(_FakeTensor("bfloat16"), "f32", "gamma")
+    with pytest.raises(TypeError, match="uint8"):
+        m(_FakeTensor("int8"), "u8", "q_out")
+    with pytest.raises(ValueError, match="different devices"):
+        m(_FakeTensor(device="cuda:1"), "bf16", "y_out")
