@@ -19,8 +19,10 @@
  *    default stream), on the device that owns the stream; every buffer must live on
  *    (or be accessible from) that device.  If the stream's device is not the calling
  *    thread's current device, the call makes it current for the launch and restores
- *    the caller's device before returning.  A returned LB_OK means the launch was
- *    enqueued.
+ *    the caller's device before returning.  While the stream is being captured into
+ *    a CUDA graph its device cannot be queried, and the call then launches on the
+ *    current device: capture on a stream of the current device.  A returned LB_OK
+ *    means the launch was enqueued.
  *  - Arithmetic ("Residual update and input read": the fused add+norm keeps its FP32
  *    accumulation and normalises it, not a rounded snapshot):
  *      o[t,h]  = (+0 + p_0[t,h] + p_1[t,h] + ... + p_{K-1}[t,h]) + res[t,h]

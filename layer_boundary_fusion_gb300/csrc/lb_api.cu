@@ -112,15 +112,26 @@ int device_info(int dev, DeviceInfo *out) {
 
 // The launch goes to the device that owns `stream` (the current device for the legacy
 // and per-thread default streams); while it is made, that device is current, and the
-// caller's current device is restored afterwards.
+// caller's current device is restored afterwards.  A stream that is being captured
+// into a CUDA graph cannot be asked for its device (cudaStreamGetDevice fails with
+// cudaErrorStreamCaptureUnsupported and invalidates the capture), so a capturing
+// stream is taken to belong to the current device.
 struct StreamDevice {
     int stream_dev = 0;
     int prev_dev = 0;
     bool switched = false;
     int open(cudaStream_t stream) {
         cudaError_t e = cudaGetDevice(&prev_dev);
-        if (e == cudaSuccess)
-            e = cudaStreamGetDevice(stream, &stream_dev);
+        stream_dev = prev_dev;
+        const bool default_stream = stream == nullptr || stream == cudaStreamLegacy ||
+                                    stream == cudaStreamPerThread;
+        if (e != cudaSuccess || default_stream)
+            return static_cast<int>(e);
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        e = cudaStreamIsCapturing(stream, &cap);
+        if (e != cudaSuccess || cap != cudaStreamCaptureStatusNone)
+            return static_cast<int>(e);
+        e = cudaStreamGetDevice(stream, &stream_dev);
         if (e == cudaSuccess && stream_dev != prev_dev) {
             e = cudaSetDevice(stream_dev);
             switched = e == cudaSuccess;

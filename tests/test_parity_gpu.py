@@ -870,3 +870,57 @@ def test_fp8_read_of_near_zero_rows(lb):
         want = oracle.fold_norm(P, R, w.gamma, w.eps, want_y=False, want_fp8=True)
         got = gpu_fold(lb, P, R, w.gamma, w.eps, want_y=False, fp8=True)
         check_fold(got, want, f"near-zero rows T={T}")
+
+
+@pytest.mark.parametrize("mode", ["global", "thread_local", "relaxed"])
+def test_calls_captured_into_a_graph(lb, mode):
+    """Every call kind captured into a CUDA graph on a side stream (a capturing stream
+    cannot be asked for its device) and replayed twice: the replays write what the
+    oracle computes, on the row kernel (T=64), the stream kernel (T=300) and the MoE
+    finalize."""
+    wr = wl.fold_workload("cap_row", 3, 64, 2048, seed=31)
+    ws = wl.fold_workload("cap_stream", 2, 300, 2048, seed=32, fp8=True)
+    wm = wl.moe_workload("cap_moe", 200, 2048, 16, 2, seed=33)
+    want_r = oracle.fold_norm(wr.partials, wr.residual, wr.gamma, wr.eps)
+    want_s = oracle.fold_norm(ws.partials, ws.residual, ws.gamma, ws.eps, want_y=False,
+                              want_fp8=True)
+    want_m = oracle.moe_finalize_fold_norm(wm.expert_out, wm.idx, wm.w, wm.residual, wm.gamma,
+                                            wm.eps)
+    Pr = [dev_bits(p) for p in wr.partials]
+    Rr = dev_bits(wr.residual)
+    Gr = torch.from_numpy(wr.gamma).cuda()
+    ror, yor = torch.empty_like(Rr), torch.empty_like(Rr)
+    Ps = [dev_bits(p) for p in ws.partials]
+    Rs = dev_bits(ws.residual)
+    Gs = torch.from_numpy(ws.gamma).cuda()
+    ros = torch.empty_like(Rs)
+    qs = torch.empty((ws.T, ws.H), dtype=torch.uint8, device="cuda")
+    ss = torch.empty((ws.T,), dtype=torch.float32, device="cuda")
+    E = dev_bits(wm.expert_out)
+    idx = torch.from_numpy(wm.idx).cuda()
+    wt = torch.from_numpy(wm.w).cuda()
+    Rm = dev_bits(wm.residual)
+    Gm = torch.from_numpy(wm.gamma).cuda()
+    rom, yom = torch.empty_like(Rm), torch.empty_like(Rm)
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cap, capture_error_mode=mode):
+        lb.lb_fold_norm(Pr, Rr, ror, Gr, yor, wr.T, wr.H, wr.eps)
+        lb.lb_fold_norm_fp8(Ps, Rs, ros, Gs, qs, ss, None, ws.T, ws.H, ws.eps)
+        lb.lb_moe_finalize_fold_norm(E, wm.expert_out.shape[0], idx, wt, wm.topk, Rm, rom, Gm, yom,
+                                     None, None, wm.T, wm.H, wm.eps)
+    for _ in range(2):
+        for t in (ror, yor, ros, rom, yom):
+            t.view(torch.int16).fill_(SENTINEL16)
+        qs.fill_(0x7F)
+        ss.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert_bits_equal(host_bits(ror), want_r["residual_out"], "captured row residual'")
+        assert_bf16_close(host_bits(yor), want_r["y"], "captured row y")
+        assert_bits_equal(host_bits(ros), want_s["residual_out"], "captured stream residual'")
+        assert_fp8_close(qs.cpu().numpy(), want_s["q"], ss.cpu().numpy(), want_s["scale"],
+                         "captured stream fp8")
+        assert_bf16_close(host_bits(rom), want_m["residual_out"], "captured moe residual'")
+        assert_bf16_close(host_bits(yom), want_m["y"], "captured moe y")
