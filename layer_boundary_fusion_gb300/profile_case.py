@@ -2,8 +2,11 @@
 
     python -m layer_boundary_fusion_gb300.profile_case prefill_fold_norm_fp8 \
         --launches 4 [--row-scale 3] [--sets 2] [--hidden 12288]
+    python -m layer_boundary_fusion_gb300.profile_case ragged_slice [--rsv-rank 1]
 
-Builds the seeded workload (the prefill one optionally at another hidden size),
+Builds the seeded workload (the prefill one optionally at another hidden size; for the
+ragged batch, with --rsv-rank, one rank's rows under the variable-size reduce-scatter
+instead of slice 3 of 8),
 optionally repeats its rows `--row-scale` times (so that a capture's working set
 exceeds the L2 cache), and launches the boundary call
 `--launches` times, rotating over `--sets` independent buffer sets.  Prints the mean
@@ -26,7 +29,7 @@ def _bits(a, dev):
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
 
 
-def make_launcher(name, row_scale, dev, stream, hidden=None):
+def make_launcher(name, row_scale, dev, stream, hidden=None, rsv_rank=None):
     w = wl.prefill_fold_norm_fp8(H=hidden) if hidden else wl.WORKLOADS[name]()
     sp = stream.cuda_stream
     G = torch.from_numpy(w.gamma).to(dev)
@@ -43,6 +46,15 @@ def make_launcher(name, row_scale, dev, stream, hidden=None):
         return T, lambda: lb.lb_moe_finalize_fold_norm(
             E, n_rows * row_scale, idx, wt, w.topk, R, ro, G, yo, None, None, T, w.H, w.eps,
             None, stream=sp)
+    if name == "ragged_slice" and rsv_rank is not None:
+        P = [_bits(p, dev) for p in w.partials]
+        rows = int(w.set_counts[rsv_rank])
+        o = int(w.set_offsets[rsv_rank])
+        R = _bits(w.residual_full[o:o + rows], dev)
+        ro, yo = torch.empty_like(R), torch.empty_like(R)
+        return rows, lambda: lb.lb_slice_fold_norm_v(
+            P, w.T_pad, rsv_rank, w.set_offsets, w.set_counts, R, ro, G, yo, None, None,
+            w.H, w.eps, stream=sp)
     if name == "ragged_slice":
         P = [_bits(p, dev) for p in w.partials]
         R = _bits(w.residual, dev)
@@ -70,13 +82,18 @@ def main(argv=None):
     ap.add_argument("--sets", type=int, default=2)
     ap.add_argument("--hidden", type=int, default=None,
                     help="prefill_fold_norm_fp8 only: hidden size (default 4096)")
+    ap.add_argument("--rsv-rank", type=int, default=None, choices=range(4),
+                    help="ragged_slice only: this rank's rows under the variable-size "
+                         "reduce-scatter instead of slice 3")
     a = ap.parse_args(argv)
     if a.hidden is not None and a.workload != "prefill_fold_norm_fp8":
         ap.error("--hidden applies to prefill_fold_norm_fp8 only")
+    if a.rsv_rank is not None and a.workload != "ragged_slice":
+        ap.error("--rsv-rank applies to ragged_slice only")
     dev = torch.device("cuda", 0)
     lb.load()
     stream = torch.cuda.Stream(dev)
-    runs = [make_launcher(a.workload, a.row_scale, dev, stream, a.hidden)
+    runs = [make_launcher(a.workload, a.row_scale, dev, stream, a.hidden, a.rsv_rank)
             for _ in range(a.sets)]
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
