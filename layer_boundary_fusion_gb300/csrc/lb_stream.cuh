@@ -686,15 +686,29 @@ __global__ void __launch_bounds__(StreamThreads<kVpt>::value, 1)
             }
             return;
         }
-        // the group's W (even) slots, two per 16-byte read, summed in warp order
+        // the group's W (even, at most 16) slots, two per 16-byte read, summed in warp
+        // order: passes of four reads, each pass's reads issued before its first add (a
+        // missing pair adds +0, which leaves the sum bit for bit as it is)
+        static_assert(kMaxGroupWarps <= 16, "two passes of four pairs");
         const float4 *slots = reinterpret_cast<const float4 *>(&red[g][par][0]);
         ss = 0.0f;
         mg = 0.0f;
-        for (int w = 0; w < (W >> 1); ++w) {
-            const float4 t = slots[w];
-            ss += t.x;
-            ss += t.z;
-            mg = fmaxf(mg, fmaxf(t.y, t.w));
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            if (8 * h >= W)
+                break;
+            float4 pair[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int w = 4 * h + i;
+                pair[i] = (w < (W >> 1)) ? slots[w] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                ss += pair[i].x;
+                ss += pair[i].z;
+                mg = fmaxf(mg, fmaxf(pair[i].y, pair[i].w));
+            }
         }
         par ^= 1;
         const float r = rsqrtf(__fmaf_rn(ss, p.inv_H, p.eps));
